@@ -1,0 +1,151 @@
+"""fp64 CPU oracle for causal multi-head attention — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never imports it, and it imports nothing from the product.
+
+The arithmetic lives in ``attention_ref.c`` (plain C, double precision,
+pthreads across rows); this module compiles it with gcc and marshals numpy
+arrays to it.  What it computes is the definition on the page "Hand-written
+masked multi-head attention CUDA kernel: underlying logic and practice",
+section 2 (A = softmax(QK^T/sqrt(d_k) + M), O = A V with M = -inf above the
+diagonal), with the valid-key rule j <= i of its section 2.2.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(brute force at high precision, closed forms, invariants, a library softmax)
+and by ``tests/test_oracle_mutants.py`` (planted mistakes must fail a pin).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_ref.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# gcc flags: no fast-math and no FMA contraction, so the double arithmetic is
+# the plain IEEE sequence written in the source on x86-64 and aarch64 alike.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
+    """Compile the oracle C source into a shared library and return its path."""
+    cmd = ["gcc", *CFLAGS, *extra_flags, "-o", out + ".tmp", src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _declare(lib):
+    f64p = ctypes.POINTER(ctypes.c_double)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    intp = ctypes.POINTER(ctypes.c_int)
+    lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = [
+        f32p, f32p, f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_double, ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, ctypes.c_int, intp]
+    lib.oracle_decode.restype = ctypes.c_int
+    lib.oracle_decode.argtypes = [
+        f32p, f32p, f32p, i32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_double, f64p, f64p, ctypes.c_int, intp]
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load (building first when missing or stale) the oracle library."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            stale = (not os.path.exists(_LIB_PATH)
+                     or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+            if stale:
+                build()
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _f32(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+class OracleResult(tuple):
+    """(O, LSE) plus the number of host threads the evaluation used."""
+    threads: int
+
+
+def attention(Q, K, V, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None):
+    """Prefill attention in fp64.
+
+    Q, K, V: float arrays [B, H, S, D] (bf16 inputs are passed as the float32
+    values they represent exactly).  ``rows``: optional flat row ids
+    (b*H + h)*S + i.  Returns (O, LSE): O [B,H,S,D] and LSE [B,H,S] in float64
+    when ``rows`` is None, else O [len(rows), D] and LSE [len(rows)].
+    """
+    lib = lib or load_library()
+    Q, qp = _f32(Q)
+    K, kp = _f32(K)
+    V, vp = _f32(V)
+    B, H, S, D = Q.shape
+    assert K.shape == Q.shape and V.shape == Q.shape
+    if rows is None:
+        n = B * H * S
+        rows_arr, rp = None, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.size
+        rp = rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    O = np.empty((n, D), dtype=np.float64)
+    LSE = np.empty((n,), dtype=np.float64)
+    used = ctypes.c_int(0)
+    rc = lib.oracle_attention_rows(
+        qp, kp, vp, B, H, S, D, float(scale), int(bool(causal)), rp, n,
+        O.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+        LSE.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nthreads), ctypes.byref(used))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_rows failed with status {rc}")
+    if rows is None:
+        O = O.reshape(B, H, S, D)
+        LSE = LSE.reshape(B, H, S)
+    res = OracleResult((O, LSE))
+    res.threads = used.value
+    return res
+
+
+def decode(q, Kc, Vc, seqlens, scale: float, nthreads: int = 0, lib=None):
+    """Single-query decode in fp64.
+
+    q: [B, H, D]; Kc, Vc: packed [sum(seqlens), H, D]; seqlens: int [B].
+    Returns (O [B,H,D], LSE [B,H]) in float64.
+    """
+    lib = lib or load_library()
+    q, qp = _f32(q)
+    Kc, kp = _f32(Kc)
+    Vc, vp = _f32(Vc)
+    B, H, D = q.shape
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    assert sl.shape == (B,)
+    assert Kc.shape == (int(sl.sum()), H, D) and Vc.shape == Kc.shape
+    O = np.empty((B, H, D), dtype=np.float64)
+    LSE = np.empty((B, H), dtype=np.float64)
+    used = ctypes.c_int(0)
+    rc = lib.oracle_decode(
+        qp, kp, vp, sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, H, D, float(scale),
+        O.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+        LSE.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nthreads), ctypes.byref(used))
+    if rc != 0:
+        raise RuntimeError(f"oracle_decode failed with status {rc}")
+    res = OracleResult((O, LSE))
+    res.threads = used.value
+    return res

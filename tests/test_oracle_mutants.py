@@ -1,0 +1,49 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Each mutant is a one-line textual change to ``oracle/attention_ref.c`` of the
+kind a careless restatement of the formula could make; the copy is compiled
+into a temporary directory, the committed oracle is untouched.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attention_ref.c")
+
+MUTANTS = {
+    "dropped_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "exponent_sign": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
+    "diagonal_excluded": ("jb->causal ? i + 1 : jb->S", "jb->causal ? (i > 0 ? i : 1) : jb->S"),
+    "mask_ignored": ("jb->causal ? i + 1 : jb->S", "jb->S"),
+    "keys_as_values": ("o[d] += a * (double)V[j * D + d];", "o[d] += a * (double)K[j * D + d];"),
+    "feature_index_reversed": ("dot += (double)q[d] * (double)K[j * D + d];",
+                               "dot += (double)q[d] * (double)K[j * D + (D - 1 - d)];"),
+    "no_normalisation": ("double a = s[j] / Z;", "double a = s[j];"),
+    "lse_without_max": ("*lse = m + log(Z);", "*lse = log(Z);"),
+    "max_not_subtracted_from_lse": ("*lse = m + log(Z);", "*lse = m * 0.5 + log(Z);"),
+    "decode_ignores_sequence_offset": ("jb->Kc + ((jb->offs[b] + t) * H + h) * D",
+                                       "jb->Kc + ((t) * H + h) * D"),
+    "decode_value_offset": ("jb->Vc + ((jb->offs[b] + t) * H + h) * D",
+                            "jb->Vc + ((jb->offs[b] + t) * H + (H - 1 - h)) * D"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "attention_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.load_library(oracle.build(str(mutated), str(tmp_path / "libmutant.so")))
+    caught = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(lib)
+        except AssertionError:
+            caught.append(check.__name__)
+            break
+    assert caught, f"no pin fails for planted mistake {name}"
