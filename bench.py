@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Throughput of the fused causal MHA path on GB300, one JSON line on stdout.
+
+A step is one pass of the hot path over one batch of synthetic input:
+  * bf16 causal prefill on the large-logit workload B=4, H=32, S=4096, D=128
+    (Q, K ~ N(0, 3^2), V ~ N(0, 1)) -- one mha_fwd call, O and LSE written;
+  * bf16 single-query decode on B=16, H=32, D=128 with cached lengths drawn
+    uniformly from [512, 8192] -- one mha_decode call (split + merge).
+`value` is the prefill throughput in TFLOP/s, counting 2*B*H*S^2*D flops per
+causal call, over the prefill kernels' device time; the decode throughput
+(algorithmic bytes: K and V read once, q read and O written) is reported in
+the `decode` object.  Inputs (384 MiB for prefill, ~1.1 GiB of cache for
+decode) are larger than the 129 MB L2, so no flush is needed between steps.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on bounded samples of the same prefill workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "causal MHA prefill TFLOPS (% BF16 peak); decode mmha HBM GB/s (% peak)"
+PREFILL_WORKLOAD = "prefill_bf16_b4h32s4096d128_qk3"
+DECODE_WORKLOAD = "decode_bf16_b16h32d128_len512_8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
+# named workload, valid only while the kernel source hashes to the recorded value.
+TRAFFIC = {
+    "prefill": {"file": "causal_head_attention_mha_gb300/csrc/prefill_bf16.cu", "sha256": None,
+                "bytes_per_launch": None},
+    "decode": {"file": "causal_head_attention_mha_gb300/csrc/decode.cu", "sha256": None,
+               "bytes_per_launch": None},
+}
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_for(kernel):
+    t = TRAFFIC[kernel]
+    if t["sha256"] is None or t["bytes_per_launch"] is None:
+        return None
+    return t["bytes_per_launch"] if source_sha(t["file"]) == t["sha256"] else None
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(B, H, S, D, causal=True):
+    return (2.0 if causal else 4.0) * B * H * S * S * D
+
+
+def decode_bytes(B, H, D, seqlens):
+    return 2.0 * float(np.sum(seqlens)) * H * D * 2 + 2.0 * B * H * D * 2
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            text, _ = self.proc.communicate()
+        rows = [r.split(",") for r in text.strip().splitlines() if r.count(",") >= 8]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None):
+    """Time the fp64 oracle on random rows of the prefill workload for about target_s."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    total_rows = x.B * x.H * x.S
+    max_rows = total_rows if max_rows is None else max_rows
+
+    def run(n):
+        rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+        i = rows % x.S
+        flops = float(np.sum(4.0 * (i + 1) * x.D)) if causal else 4.0 * x.S * x.D * n
+        t0 = time.perf_counter()
+        res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows)
+        return time.perf_counter() - t0, flops, res.threads
+
+    dt, _, _ = run(64)
+    per_row = max(dt / 64, 1e-6)
+    n = int(min(max_rows, max(64, target_s / per_row)))
+    dt, flops, threads = run(n)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} random query rows of {PREFILL_WORKLOAD} (causal), "
+                      f"fp64 C oracle, {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    w = si.WORKLOADS[PREFILL_WORKLOAD]
+    x = si.workload_inputs(PREFILL_WORKLOAD)
+    rng = np.random.default_rng(123)
+    total_rows = x.B * x.H * x.S
+    budget_per_step = min(1.0, 150.0 / max(1, args.steps + args.warmup))
+
+    def step(n):
+        rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+        i = rows % x.S
+        t0 = time.perf_counter()
+        res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, True, rows=rows)
+        return time.perf_counter() - t0, float(np.sum(4.0 * (i + 1) * x.D)), res.threads
+
+    dt, _, _ = step(32)
+    n = int(max(16, min(100000, budget_per_step / max(dt / 32, 1e-6))))
+    for _ in range(args.warmup):
+        step(n)
+    tot_t = tot_f = 0.0
+    threads = 0
+    for _ in range(args.steps):
+        dt, fl, threads = step(n)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL_WORKLOAD, "B": w["B"], "H": w["H"], "S": w["S"],
+                   "D": w["D"], "causal": True, "sample_rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} random query rows per step of {PREFILL_WORKLOAD}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, dist):
+    import torch
+    import causal_head_attention_mha_gb300 as mha
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mha.load_library()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    def bf16_dev(t):
+        return torch.from_numpy(t.bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    do_prefill = args.only in ("both", "prefill")
+    do_decode = args.only in ("both", "decode")
+    wp = si.WORKLOADS[PREFILL_WORKLOAD]
+    wd = si.WORKLOADS[DECODE_WORKLOAD]
+    seed_shift = 1000 * rank  # each rank works on its own batch (weak scaling, no collective)
+    if do_prefill:
+        xp = si.prefill_inputs(wp["B"], wp["H"], wp["S"], wp["D"], wp["seed"] + seed_shift,
+                               qk_std=wp["qk_std"])
+        Q, K, V = bf16_dev(xp.Q), bf16_dev(xp.K), bf16_dev(xp.V)
+        O = torch.empty_like(Q)
+        LSE = torch.empty((xp.B, xp.H, xp.S), dtype=torch.float32, device=dev)
+        flops = prefill_flops(xp.B, xp.H, xp.S, xp.D, True)
+    if do_decode:
+        xd = si.decode_inputs(wd["B"], wd["H"], wd["D"], wd["seed"] + seed_shift, wd["len_lo"],
+                              wd["len_hi"])
+        q, Kc, Vc = bf16_dev(xd.q), bf16_dev(xd.Kc), bf16_dev(xd.Vc)
+        sl = torch.from_numpy(xd.seqlens).to(dev)
+        Od = torch.empty_like(q)
+        dbytes = decode_bytes(xd.B, xd.H, xd.D, xd.seqlens)
+        nsplit = mha.mha_decode_num_splits(xd.B, xd.H)
+
+    def prefill():
+        mha.mha_fwd(Q, K, V, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
+
+    def decode():
+        mha.mha_decode(q, Kc, Vc, sl, O=Od, scale=xd.scale, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---------------- warm-up
+    for _ in range(args.warmup):
+        if do_prefill:
+            prefill()
+        if do_decode:
+            decode()
+    barrier()
+    st = mha.mha_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {mha.mha_status_string(st)}")
+
+    # ---------------- timed region (device-resident inputs)
+    K_ = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
+    clock = ClockSampler(local)
+    if not args.profile:
+        clock.start()
+        time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(K_):
+        evs[k][0].record(stream)
+        if do_prefill:
+            prefill()
+        evs[k][1].record(stream)
+        if do_decode:
+            decode()
+        evs[k][2].record(stream)
+    t_end.record(stream)
+    barrier()
+    clocks = clock.stop() if not args.profile else None
+    st = mha.mha_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {mha.mha_status_string(st)}")
+    tp = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3  # s, prefill launches
+    td = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3  # s, decode launches
+    total = t_start.elapsed_time(t_end) / 1e3
+    times = torch.tensor([tp, td, total], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    tp, td, total = (float(v) for v in times.tolist())
+    launches = K_ * ((1 if do_prefill else 0) + ((1 + (nsplit > 1)) if do_decode else 0))
+
+    # ---------------- end to end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        E = min(K_, args.e2e_steps)
+        h2d = d2h = 0
+        if do_prefill:
+            hQ, hK, hV = (torch.from_numpy(t.bits.view(np.int16)).pin_memory()
+                          for t in (xp.Q, xp.K, xp.V))
+            hO = torch.empty(Q.shape, dtype=torch.int16).pin_memory()
+            hL = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
+            h2d += 3 * hQ.numel() * 2
+            d2h += hO.numel() * 2 + hL.numel() * 4
+        if do_decode:
+            hq = torch.from_numpy(xd.q.bits.view(np.int16)).pin_memory()
+            hKc = torch.from_numpy(xd.Kc.bits.view(np.int16)).pin_memory()
+            hVc = torch.from_numpy(xd.Vc.bits.view(np.int16)).pin_memory()
+            hsl = torch.from_numpy(xd.seqlens).pin_memory()
+            hOd = torch.empty(q.shape, dtype=torch.int16).pin_memory()
+            h2d += (hq.numel() + hKc.numel() + hVc.numel()) * 2 + hsl.numel() * 4
+            d2h += hOd.numel() * 2
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(E)]
+        barrier()
+        for k in range(E):
+            ee[k][0].record(stream)
+            if do_prefill:
+                Q.view(torch.int16).copy_(hQ, non_blocking=True)
+                K.view(torch.int16).copy_(hK, non_blocking=True)
+                V.view(torch.int16).copy_(hV, non_blocking=True)
+                prefill()
+                hO.copy_(O.view(torch.int16), non_blocking=True)
+                hL.copy_(LSE, non_blocking=True)
+            ee[k][1].record(stream)
+            if do_decode:
+                q.view(torch.int16).copy_(hq, non_blocking=True)
+                Kc.view(torch.int16).copy_(hKc, non_blocking=True)
+                Vc.view(torch.int16).copy_(hVc, non_blocking=True)
+                sl.copy_(hsl, non_blocking=True)
+                decode()
+                hOd.copy_(Od.view(torch.int16), non_blocking=True)
+            ee[k][2].record(stream)
+        barrier()
+        ep = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
+        ed = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
+        et = torch.tensor([ep, ed], dtype=torch.float64, device=dev)
+        if dist is not None:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        ep, ed = (float(v) for v in et.tolist())
+        e2e = {"value": (world * E * flops / ep / 1e12) if do_prefill else None,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": E,
+               "decode_gbs": (world * E * dbytes / ed / 1e9) if do_decode else None,
+               "path": "pinned host -> cudaMemcpyAsync -> C-ABI call -> cudaMemcpyAsync -> "
+                       "pinned host, all on one stream"}
+
+    if rank != 0:
+        return 0
+
+    line = {"impl": "ours", "metric": METRIC}
+    cfg = {"workload": PREFILL_WORKLOAD if do_prefill else DECODE_WORKLOAD,
+           "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+    if do_prefill:
+        value = world * K_ * flops / tp / 1e12
+        per_launch_s = tp / K_
+        achieved = flops / per_launch_s / 1e12
+        line.update({"value": value, "unit": "TFLOP/s"})
+        cfg.update({"prefill": {"B": xp.B, "H": xp.H, "S": xp.S, "D": xp.D, "causal": True,
+                                "qk_std": 3.0, "flops_per_step": flops}})
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                    "traffic": traffic_for("prefill"),
+                    "peak_source": f"bf16_tflops (burst), of {peak_src}",
+                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                    "kernel": "prefill_bf16_kernel<128, causal>", "us_per_launch": 1e6 * per_launch_s}
+        line["roofline"] = roofline
+    if do_decode:
+        gbs = world * K_ * dbytes / td / 1e9
+        cfg.update({"decode": {"B": xd.B, "H": xd.H, "D": xd.D, "len_range": [512, 8192],
+                               "total_tokens": int(xd.seqlens.sum()), "splits": nsplit,
+                               "bytes_per_step": dbytes}})
+        line["decode"] = {"value": gbs, "unit": "GB/s", "bound": "hbm",
+                          "achieved": dbytes / (td / K_) / 1e9, "peak": peaks["hbm_gbs"],
+                          "frac": dbytes / (td / K_) / 1e9 / peaks["hbm_gbs"],
+                          "traffic": traffic_for("decode"), "peak_source": f"hbm_gbs, of {peak_src}",
+                          "us_per_call": 1e6 * td / K_}
+        if not do_prefill:
+            line.update({"value": gbs, "unit": "GB/s"})
+    line.update({
+        "n_gpus": world, "steps": K_, "warmup": args.warmup, "ms_per_step": 1e3 * total / K_,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": cfg, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": launches,
+    })
+    if not args.no_cpu_baseline and world == 1 and do_prefill:
+        line["cpu_baseline"] = oracle_sample_tflops(xp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--only", choices=("both", "prefill", "decode"), default="both")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile", action="store_true", help="no clock sampling (for ncu runs)")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.profile:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        return run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+"""ctypes binding of libmha.so: argument marshalling only.
+
+Every function here checks the torch tensors it is given (device, dtype,
+shape, contiguity), passes their device pointers and the current CUDA stream
+to the C entry point of the same name, and raises :class:`MHAError` on a
+non-zero status.  All arithmetic happens in the library's CUDA kernels;
+there is no fallback of any kind: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libmha.so")
+_lib = None
+_lock = threading.Lock()
+
+MHA_OK = 0
+STATUS_NAMES = {0: "MHA_OK", 1: "MHA_ERR_INVALID_ARG", 2: "MHA_ERR_UNSUPPORTED",
+                3: "MHA_ERR_MISALIGNED", 4: "MHA_ERR_CUDA", 5: "MHA_ERR_TIMEOUT"}
+
+
+class MHAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        text = _load().mha_status_string(status).decode()
+        extra = ""
+        if status == 4:
+            extra = f" (cudaError {_load().mha_last_cuda_error()})"
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {text}{extra}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _declare(lib):
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.mha_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.mha_fwd.restype = i
+    lib.mha_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.mha_fwd_f32.restype = i
+    lib.mha_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
+    lib.mha_decode.restype = i
+    lib.mha_decode_num_splits.argtypes = [i, i]
+    lib.mha_decode_num_splits.restype = i
+    lib.mha_get_device_status.argtypes = [vp]
+    lib.mha_get_device_status.restype = i
+    lib.mha_status_string.argtypes = [i]
+    lib.mha_status_string.restype = ctypes.c_char_p
+    lib.mha_last_cuda_error.argtypes = []
+    lib.mha_last_cuda_error.restype = i
+    lib.mha_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.mha_set_wait_limit_ns.restype = ctypes.c_uint64
+    lib.mha_set_fault_injection.argtypes = [i]
+    lib.mha_set_fault_injection.restype = i
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load libmha.so; raises if it has not been built."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+_load = load_library
+
+
+def _stream_ptr(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device or t.device.type != "cuda":
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _prefill(entry, dtype, Q, K, V, O, LSE, scale, causal, stream, want_lse):
+    if Q.dim() != 4:
+        raise ValueError("Q must be [B, H, S, D]")
+    B, H, S, D = Q.shape
+    dev = Q.device
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _check(t, name, dtype, (B, H, S, D), dev)
+    if O is None:
+        O = torch.empty_like(Q)
+    _check(O, "O", dtype, (B, H, S, D), dev)
+    if LSE is None and want_lse:
+        LSE = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    if LSE is not None:
+        _check(LSE, "LSE", torch.float32, (B, H, S), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = getattr(_load(), entry)(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                 LSE.data_ptr() if LSE is not None else None,
+                                 B, H, S, D, float(scale), int(bool(causal)),
+                                 _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, entry)
+    return O, LSE
+
+
+def mha_fwd(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, want_lse=True):
+    """bf16 [B,H,S,D] prefill; returns (O, LSE).  See include/mha.h: mha_fwd."""
+    return _prefill("mha_fwd", torch.bfloat16, Q, K, V, O, LSE, scale, causal, stream, want_lse)
+
+
+def mha_fwd_f32(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, want_lse=True):
+    """float32 [B,H,S,D] prefill; returns (O, LSE).  See include/mha.h: mha_fwd_f32."""
+    return _prefill("mha_fwd_f32", torch.float32, Q, K, V, O, LSE, scale, causal, stream,
+                    want_lse)
+
+
+def mha_decode(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
+    """bf16 single-query decode over a packed cache; returns O [B,H,D].
+
+    q: [B,H,D]; Kcache, Vcache: [sum(seqlens), H, D]; seqlens: int32 [B] on the device.
+    """
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, D]")
+    B, H, D = q.shape
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (B, H, D), dev)
+    if Kcache.dim() != 3 or Kcache.shape[1:] != (H, D):
+        raise ValueError("Kcache must be [total_tokens, H, D]")
+    _check(Kcache, "Kcache", torch.bfloat16, tuple(Kcache.shape), dev)
+    _check(Vcache, "Vcache", torch.bfloat16, tuple(Kcache.shape), dev)
+    _check(seqlens, "seqlens", torch.int32, (B,), dev)
+    if O is None:
+        O = torch.empty_like(q)
+    _check(O, "O", torch.bfloat16, (B, H, D), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = _load().mha_decode(q.data_ptr(), Kcache.data_ptr(), Vcache.data_ptr(), seqlens.data_ptr(),
+                            O.data_ptr(), B, H, D, float(scale), _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, "mha_decode")
+    return O
+
+
+def mha_decode_num_splits(B: int, H: int) -> int:
+    """Key splits (partials merged by a second kernel) mha_decode uses on this device."""
+    n = _load().mha_decode_num_splits(int(B), int(H))
+    if n <= 0:
+        raise MHAError(4, "mha_decode_num_splits")
+    return n
+
+
+def mha_get_device_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device wait status."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return _load().mha_get_device_status(_stream_ptr(stream, dev))
+
+
+def mha_status_string(status: int) -> str:
+    return _load().mha_status_string(int(status)).decode()
+
+
+def mha_set_wait_limit_ns(limit_ns: int) -> int:
+    return int(_load().mha_set_wait_limit_ns(int(limit_ns)))
+
+
+def mha_set_fault_injection(mode: int) -> int:
+    """Failure-detection hook (see include/mha.h); returns the previous mode."""
+    return int(_load().mha_set_fault_injection(int(mode)))

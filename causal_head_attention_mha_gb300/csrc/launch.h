@@ -1,0 +1,35 @@
+// launch.h — host-side launchers of the kernels, shared by the C-ABI layer.
+// Each returns a cudaError_t; argument validation happens before in mha_api.cu.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mha {
+
+// Default and drain limits of the bounded device waits (nanoseconds).
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                int B, int H, int S, int D, float scale, int causal,
+                                cudaStream_t stream, uint64_t wait_limit_ns, int inject);
+
+cudaError_t launch_prefill_f32(const float* Q, const float* K, const float* V, float* O,
+                               float* LSE, int B, int H, int S, int D, float scale, int causal,
+                               cudaStream_t stream);
+
+// Number of key splits mha_decode uses for a given batch and head count.
+int decode_num_splits(int B, int H, int num_sms);
+
+// Partials of the key splits go to `ws` (B*H*nsplit*(D+2) floats, ignored when nsplit == 1).
+cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, const int* seqlens,
+                          void* O, float* ws, int B, int H, int D, int nsplit, float scale,
+                          cudaStream_t stream);
+
+// Reads and clears the device error word of the prefill translation unit.
+cudaError_t take_prefill_bf16_error(unsigned int* word);
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace mha

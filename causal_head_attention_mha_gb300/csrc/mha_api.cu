@@ -1,0 +1,148 @@
+// mha_api.cu — the extern "C" boundary of libmha.so (declared in include/mha.h).
+//
+// Host-side only: argument and alignment checks (page "CUDA depthwise
+// convolution" section 6.2 checks shapes at the entry point; section 3.2
+// checks the launch status right after each launch), the choice of kernel,
+// stream-ordered scratch for the decode splits, and the device error word
+// that bounded waits set.
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mha.h"
+#include "launch.h"
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{mha::kDefaultWaitLimitNs};
+std::atomic<int> g_last_cuda_error{0};
+std::atomic<int> g_fault_injection{0};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error.store(static_cast<int>(e));
+  cudaGetLastError();  // clear a sticky-free error so later calls start clean
+  return MHA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_prefill(const void* Q, const void* K, const void* V, const void* O, const void* LSE,
+                  int B, int H, int S, int D, float scale, int causal) {
+  if (!Q || !K || !V || !O) return MHA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || D < 1) return MHA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return MHA_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || scale == INFINITY) return MHA_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(B) * H * S * D;
+  if (n >= (1LL << 31)) return MHA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return MHA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return MHA_ERR_MISALIGNED;
+  if (LSE && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return MHA_ERR_MISALIGNED;
+  return MHA_OK;
+}
+
+}  // namespace
+
+namespace mha {
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+}  // namespace mha
+
+extern "C" {
+
+int mha_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int S,
+            int D, float scale, int causal, void* stream) {
+  const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
+  if (st != MHA_OK) return st;
+  const cudaError_t e =
+      mha::launch_prefill_bf16(Q, K, V, O, LSE, B, H, S, D, scale, causal,
+                               static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
+                               g_fault_injection.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE, int B,
+                int H, int S, int D, float scale, int causal, void* stream) {
+  const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
+  if (st != MHA_OK) return st;
+  const cudaError_t e = mha::launch_prefill_f32(Q, K, V, O, LSE, B, H, S, D, scale, causal,
+                                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int* seqlens, void* O,
+               int B, int H, int D, float scale, void* stream) {
+  if (!q || !Kcache || !Vcache || !seqlens || !O) return MHA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || D < 1) return MHA_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || scale == INFINITY) return MHA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * D >= (1LL << 31) || B > 65535 || H > 65535)
+    return MHA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return MHA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(Kcache) || !aligned16(Vcache) || !aligned16(O))
+    return MHA_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(seqlens) & 3u) return MHA_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nsm = mha::device_sm_count();
+  if (nsm <= 0) return cuda_fail(cudaGetLastError());
+  const int nsplit = mha::decode_num_splits(B, H, nsm);
+  float* ws = nullptr;
+  if (nsplit > 1) {
+    const size_t bytes = static_cast<size_t>(B) * H * nsplit * (D + 2) * sizeof(float);
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  cudaError_t e = mha::launch_decode(q, Kcache, Vcache, seqlens, O, ws, B, H, D, nsplit, scale, s);
+  if (ws) {
+    const cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = ef;
+  }
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+int mha_decode_num_splits(int B, int H) {
+  if (B < 1 || H < 1) return 0;
+  const int nsm = mha::device_sm_count();
+  if (nsm <= 0) return -1;
+  return mha::decode_num_splits(B, H, nsm);
+}
+
+int mha_get_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int word = 0;
+  e = mha::take_prefill_bf16_error(&word);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return word ? MHA_ERR_TIMEOUT : MHA_OK;
+}
+
+const char* mha_status_string(int status) {
+  switch (status) {
+    case MHA_OK: return "ok";
+    case MHA_ERR_INVALID_ARG: return "invalid argument";
+    case MHA_ERR_UNSUPPORTED: return "unsupported configuration (head dim must be 64 or 128)";
+    case MHA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case MHA_ERR_CUDA: return "CUDA error";
+    case MHA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int mha_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+uint64_t mha_set_wait_limit_ns(uint64_t limit_ns) {
+  return g_wait_limit_ns.exchange(limit_ns ? limit_ns : mha::kDefaultWaitLimitNs);
+}
+
+int mha_set_fault_injection(int mode) {
+  if (mode != 0 && mode != 1) return -1;
+  return g_fault_injection.exchange(mode);
+}
+
+}  // extern "C"

@@ -1,0 +1,150 @@
+/*
+ * mha.h — C ABI of libmha.so: fused causal multi-head attention forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the masked multi-head attention of the page "Hand-written
+ * masked multi-head attention CUDA kernel: underlying logic and practice"
+ * (xdnf.cn/news/357253), section 2:
+ *
+ *     O = softmax(scale * Q K^T + M) V,   M[i][j] = 0 if j <= i, -inf otherwise
+ *
+ * (the page prints the last product as "A V^T"; A V is the product whose
+ * dimensions agree, and it is what these calls compute).  Section 2.2 of that
+ * page fuses the score GEMV, the softmax and the product with V so that
+ * scores and probabilities never reach global memory; every call here works
+ * that way.  The single-pass running-max/running-sum softmax follows the
+ * online-softmax recurrence of the page "Week 4 CUDA notes"
+ * (pnsm.cn/news/1831385), section 2.2.
+ *
+ * Conventions shared by every call:
+ *   - Tensors are owned by the caller and live in device memory, contiguous,
+ *     with the shapes stated per call.  Every tensor pointer must be 16-byte
+ *     aligned (MHA_ERR_MISALIGNED otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL means the legacy default stream).  None synchronises the host.
+ *   - A call returns MHA_OK or an mha_status.  Argument errors are found on the
+ *     host before anything is launched; a launch error is reported as
+ *     MHA_ERR_CUDA (the CUDA error is cleared and kept for mha_last_cuda_error).
+ *   - Device-side waits inside the kernels are bounded in time; a wait that
+ *     runs out sets a device error word instead of hanging, and
+ *     mha_get_device_status reports it as MHA_ERR_TIMEOUT.
+ *   - LSE, where written, is the natural log of the softmax denominator of
+ *     each row: ln(sum over valid keys j of exp(scale * q_i . k_j)), float32.
+ */
+#ifndef MHA_GB300_H
+#define MHA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, size overflow   */
+    MHA_ERR_UNSUPPORTED = 2,  /* valid but not built: e.g. head dim not 64 or 128 */
+    MHA_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned          */
+    MHA_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed    */
+    MHA_ERR_TIMEOUT = 5       /* a bounded device wait ran out (see above)        */
+} mha_status;
+
+/*
+ * Causal (or full) attention prefill, bf16 in and out, fp32 accumulation.
+ * Page 3, section 2 (definition) and section 2.2 (fusion and mask j <= i).
+ *
+ *   Q, K, V : const bf16 [B, H, S, D], contiguous (S query rows = S key rows).
+ *   O       : bf16 [B, H, S, D], written.
+ *   LSE     : float [B, H, S], written; may be NULL to skip it.
+ *   B, H, S : >= 1, with B*H*S*D < 2^31.   D : 64 or 128.
+ *   scale   : multiplies Q.K before the mask (1/sqrt(D) for standard attention).
+ *   causal  : 1 = key j is used by query i only when j <= i; 0 = every key.
+ *   stream  : cudaStream_t.
+ *
+ * Scores and probabilities stay on chip.  The probabilities are rounded to
+ * bf16 before the product with V (the page's section 3.3 stores the operands
+ * in 16 bits and accumulates in fp32).  Returns MHA_OK or an mha_status.
+ */
+int mha_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+            int B, int H, int S, int D, float scale, int causal, void* stream);
+
+/*
+ * The same operation with float32 inputs and outputs, computed in fp32 on
+ * the CUDA cores (no reduced-precision tensor-core arithmetic anywhere).
+ * Arguments as mha_fwd, with Q, K, V, O float [B, H, S, D].  D : 64 or 128.
+ */
+int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
+                int B, int H, int S, int D, float scale, int causal, void* stream);
+
+/*
+ * Single-query decode ("mmha"): for every sequence b and head h one query
+ * attends to all cached keys of sequence b.  Page 3, sections 2.1-2.2 (one
+ * query row against a K tile, fused GEMV + softmax), with the key range split
+ * across thread blocks and merged with a log-sum-exp combine, the
+ * cross-block normalisation that page 1 section 2.2 warns must not be done
+ * per block.
+ *
+ *   q       : const bf16 [B, H, D].
+ *   Kcache,
+ *   Vcache  : const bf16 [sum_b seqlens[b], H, D]: the sequences packed back
+ *             to back, token t of sequence b at row (sum_{b'<b} seqlens[b'] + t).
+ *   seqlens : const int32 [B] in DEVICE memory, each >= 0; a sequence of length
+ *             0 gets O = 0.
+ *   O       : bf16 [B, H, D], written.
+ *   B, H    : >= 1.  D : 64 or 128.  scale as in mha_fwd.
+ *
+ * Scratch: the partial results of the key splits (B*H*nsplit*(D+2) floats)
+ * are allocated and freed stream-ordered on `stream` (cudaMallocAsync /
+ * cudaFreeAsync from the device's default memory pool) inside the call.
+ */
+int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
+               void* O, int B, int H, int D, float scale, void* stream);
+
+/*
+ * Number of key splits mha_decode uses for B sequences x H heads on the
+ * current device (1 means no merge kernel and no scratch).  The scratch of
+ * one mha_decode call is B*H*splits*(D+2)*4 bytes.  Returns <= 0 on a CUDA
+ * error or an invalid argument.
+ */
+int mha_decode_num_splits(int B, int H);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * bounded waits set.  Returns MHA_OK, MHA_ERR_TIMEOUT when a wait in some
+ * kernel of this library ran out since the last call, or MHA_ERR_CUDA when
+ * the synchronisation itself failed.
+ */
+int mha_get_device_status(void* stream);
+
+/* Static, human-readable text for an mha_status value. */
+const char* mha_status_string(int status);
+
+/* The cudaError_t value of the last call that returned MHA_ERR_CUDA (0 if none). */
+int mha_last_cuda_error(void);
+
+/*
+ * Failure-detection hook: sets the time limit, in nanoseconds, of every
+ * bounded device wait in later launches (default 2e9 = 2 s; 0 restores the
+ * default).  A tiny limit makes waits run out on purpose so that the
+ * timeout path — error word set, in-flight copies drained, tensor memory
+ * freed, kernel returns — can be exercised without hanging anything.
+ * Returns the previous limit.
+ */
+uint64_t mha_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Failure-detection hook: mode 1 makes later mha_fwd launches withhold one
+ * internal signal (each CTA's first "probabilities ready" arrival), a signal
+ * that then never comes, so the bounded wait for it runs out; the kernel
+ * records MHA_ERR_TIMEOUT, lets its in-flight copies and tensor-core work
+ * finish, frees its tensor memory and returns.  Outputs of such a launch are
+ * undefined.  Mode 0 (the default) turns it off.  Returns the previous mode,
+ * or -1 for an unknown mode.
+ */
+int mha_set_fault_injection(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_GB300_H */

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads without a GPU and exports what mha.h declares.
+
+Also checks the host-side argument validation, which returns before any CUDA
+call (no compute call is made here: these tests run on machines without a GPU).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mha.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+FAKE = 0x10000  # an aligned address that is never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_head_attention_mha_gb300 import build
+    build.build()
+    from causal_head_attention_mha_gb300 import binding
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mha_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("mha_fwd", "mha_fwd_f32", "mha_decode", "mha_get_device_status",
+                     "mha_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_needs_no_driver_at_load_time(lib):
+    from causal_head_attention_mha_gb300 import binding
+    # loading a second handle with the dynamic loader directly must also work
+    ctypes.CDLL(binding.library_path())
+
+
+def fwd(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, LSE=None, B=1, H=2, S=128, D=64, scale=0.125,
+             causal=1, stream=None)
+    a.update(kw)
+    return lib.mha_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["S"], a["D"],
+                       a["scale"], a["causal"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(Q=None), INVALID), (dict(O=None), INVALID), (dict(B=0), INVALID), (dict(H=-1), INVALID),
+    (dict(S=0), INVALID), (dict(D=0), INVALID), (dict(scale=0.0), INVALID),
+    (dict(scale=-0.1), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID), (dict(causal=2), INVALID),
+    (dict(B=1 << 12, H=1 << 12, S=1 << 12, D=64), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
+    (dict(Q=FAKE + 8), MISALIGNED), (dict(V=FAKE + 2), MISALIGNED), (dict(O=FAKE + 4), MISALIGNED),
+    (dict(LSE=FAKE + 2), MISALIGNED),
+])
+def test_prefill_validation(lib, kw, expected):
+    assert fwd(lib, **kw) == expected
+    f32 = dict(kw)
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, LSE=None, B=1, H=2, S=128, D=64, scale=0.125,
+             causal=1, stream=None)
+    a.update(f32)
+    assert lib.mha_fwd_f32(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["S"],
+                           a["D"], a["scale"], a["causal"], a["stream"]) == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(q=None), INVALID), (dict(seqlens=None), INVALID), (dict(B=0), INVALID),
+    (dict(H=0), INVALID), (dict(scale=0.0), INVALID), (dict(D=32), UNSUPPORTED),
+    (dict(Kc=FAKE + 8), MISALIGNED), (dict(seqlens=FAKE + 2), MISALIGNED),
+])
+def test_decode_validation(lib, kw, expected):
+    a = dict(q=FAKE, Kc=FAKE, Vc=FAKE, seqlens=FAKE, O=FAKE, B=2, H=2, D=128, scale=0.1)
+    a.update(kw)
+    assert lib.mha_decode(a["q"], a["Kc"], a["Vc"], a["seqlens"], a["O"], a["B"], a["H"], a["D"],
+                          a["scale"], None) == expected
+
+
+def test_status_strings_and_wait_limit(lib):
+    for s in range(6):
+        assert lib.mha_status_string(s)
+    assert b"unknown" in lib.mha_status_string(99)
+    assert lib.mha_set_fault_injection(1) == 0
+    assert lib.mha_set_fault_injection(7) == -1
+    assert lib.mha_set_fault_injection(0) == 1
+    old = lib.mha_set_wait_limit_ns(12345)
+    assert old == 2_000_000_000
+    assert lib.mha_set_wait_limit_ns(0) == 12345
+    assert lib.mha_set_wait_limit_ns(0) == 2_000_000_000
