@@ -47,6 +47,8 @@ def _declare(lib):
     lib.mha_fwd_f32.restype = i
     lib.mha_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
     lib.mha_decode.restype = i
+    lib.mha_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
+    lib.mha_decode_noalloc.restype = i
     lib.mha_decode_num_splits.argtypes = [i, i]
     lib.mha_decode_num_splits.restype = i
     lib.mha_get_device_status.argtypes = [vp]
@@ -159,6 +161,34 @@ def mha_decode(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
                             O.data_ptr(), B, H, D, float(scale), _stream_ptr(stream, dev))
     if st != MHA_OK:
         raise MHAError(st, "mha_decode")
+    return O
+
+
+def mha_decode_noalloc(q, Kcache, Vcache, seqlens, O, scale=None, stream=None):
+    """mha_decode with its scratch in the library's fixed device array.
+
+    Allocates nothing: the caller passes O as well.  See include/mha.h:
+    mha_decode_noalloc (size limit, first call before stream capture,
+    overlapping calls race).
+    """
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, D]")
+    B, H, D = q.shape
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (B, H, D), dev)
+    if Kcache.dim() != 3 or Kcache.shape[1:] != (H, D):
+        raise ValueError("Kcache must be [total_tokens, H, D]")
+    _check(Kcache, "Kcache", torch.bfloat16, tuple(Kcache.shape), dev)
+    _check(Vcache, "Vcache", torch.bfloat16, tuple(Kcache.shape), dev)
+    _check(seqlens, "seqlens", torch.int32, (B,), dev)
+    _check(O, "O", torch.bfloat16, (B, H, D), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = _load().mha_decode_noalloc(q.data_ptr(), Kcache.data_ptr(), Vcache.data_ptr(),
+                                    seqlens.data_ptr(), O.data_ptr(), B, H, D, float(scale),
+                                    _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, "mha_decode_noalloc")
     return O
 
 

@@ -32,4 +32,7 @@ cudaError_t take_prefill_bf16_error(unsigned int* word);
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
 
+// Keeps `e` for mha_last_cuda_error, clears it, and returns MHA_ERR_CUDA.
+int record_cuda_failure(cudaError_t e);
+
 }  // namespace mha

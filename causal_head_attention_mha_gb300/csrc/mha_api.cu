@@ -43,6 +43,8 @@ int check_prefill(const void* Q, const void* K, const void* V, const void* O, co
 }  // namespace
 
 namespace mha {
+int record_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+
 int device_sm_count() {
   static int cached[64] = {0};
   int dev = 0;

@@ -101,6 +101,36 @@ int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int*
                void* O, int B, int H, int D, float scale, void* stream);
 
 /*
+ * mha_decode without allocating anything.  This entry point has no
+ * counterpart on the pages the method comes from; it exists for callers
+ * that cannot allocate device memory when they call: a serving loop that
+ * plans all of its device memory up front and treats any later allocation
+ * as an error, a device or driver mode without memory-pool support (where
+ * the cudaMallocAsync that mha_decode uses fails), or code running while its
+ * process's own allocator is busy.
+ *
+ * Arguments, layouts and results are those of mha_decode.  The split
+ * partials go to one file-scope device array of
+ * MHA_DECODE_NOALLOC_SCRATCH_BYTES (2 MiB) that every GPU which loads the
+ * library holds until the process exits; the call itself makes no
+ * cudaMalloc/cudaFree or other allocating call.  When the partials would
+ * not fit (B*H*splits*(D+2)*4 bytes > 2 MiB, see mha_decode_num_splits) the
+ * call returns MHA_ERR_UNSUPPORTED before launching anything.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps
+ * whatever the last call left there; no part of it has to start at zero,
+ * since every slot a call reads was written earlier in that same call.
+ * Calls that overlap on the GPU (for instance on two streams) race on the
+ * array and may return wrong results: serialise them.
+ */
+#define MHA_DECODE_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+int mha_decode_noalloc(const void* q, const void* Kcache, const void* Vcache,
+                       const int* seqlens, void* O, int B, int H, int D, float scale,
+                       void* stream);
+
+/*
  * Number of key splits mha_decode uses for B sequences x H heads on the
  * current device (1 means no merge kernel and no scratch).  The scratch of
  * one mha_decode call is B*H*splits*(D+2)*4 bytes.  Returns <= 0 on a CUDA
