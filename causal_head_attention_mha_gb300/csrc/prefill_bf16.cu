@@ -12,16 +12,20 @@
 // notes" (pnsm.cn/news/1831385) section 2.2, evaluated with exp2 after
 // folding log2(e) into the scale.
 //
-// One CTA computes one 128-row query tile of one (batch, head):
-//   warp 0      TMA producer: Q tile once, then K_j and V_j tiles through
-//               an NST-deep shared-memory ring (128-byte swizzle).
-//   warp 1      TMEM allocation, then one thread issues the MMAs:
-//                 S_j  = Q K_j^T            (SS form, into one of two S buffers)
-//                 O   += P_j V_j            (TS form: P read from TMEM)
-//   warps 4..7  softmax: one thread per query row (TMEM lane), reads S_j,
-//               masks the diagonal tile, updates m and l, writes P_j as bf16
-//               into TMEM, rescales O when the reference maximum moves, and
-//               finally writes O / l (TMA store) and the log-sum-exp.
+// One CTA computes one 128-row query tile of one (batch, head), 384 threads:
+//   warp 0       TMA producer for Q (once) and the K ring
+//   warp 2       TMA producer for the V ring
+//   warp 1       TMEM allocation; one thread issues S_j = Q K_j^T (both
+//                operands from smem)
+//   warp 3       one thread issues O_h += P_j,h V_j,h for the two key halves
+//                h (A = P from TMEM, B = V from smem, MN-major); two issuers
+//                keep the tensor pipe fed while each does its bookkeeping
+//   warps 4..11  softmax, two independent warpgroups: half h owns key
+//                columns 64h..64h+63 of every tile, with its own running
+//                maximum, sums and output accumulator O_h in TMEM; it writes
+//                its half of P as bf16 into TMEM and rescales O_h when its
+//                reference maximum moves.  The epilogue merges O_0 and O_1
+//                by the log-sum-exp rule, stores O (TMA) and the log-sum-exp.
 // Key tiles above the diagonal are skipped; only the diagonal tile (causal)
 // or the ragged last tile (non-causal) is masked element by element.
 #include <cuda_runtime.h>
@@ -40,33 +44,40 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per tile
 constexpr float kLn2 = 0.69314718055994530942f;
+// one pair of exponentials in kPolyEvery goes to the FMA-pipe polynomial (0: none)
+constexpr int kPolyEvery = 0;
+constexpr int kSoftmaxThreads = 256;  // two warpgroups, warps 4..11
+constexpr int kThreads = 128 + kSoftmaxThreads;
 
 template <int D>
 struct Cfg {
   static constexpr int KB = D / 64;               // 128-byte column blocks per row
   static constexpr int BLOCK_BYTES = 128 * 128;   // one 128-row x 64-col bf16 block
   static constexpr int TILE_BYTES = KB * BLOCK_BYTES;
-  static constexpr int NST = (D == 128) ? 2 : 4;  // K/V ring depth
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = TILE_BYTES;
+  static constexpr int NST = (D == 128) ? 3 : 6;  // depth of each of the K and V rings
+  static constexpr int Q_OFF = 0;                 // Q tile (then the epilogue exchange)
+  static constexpr int K_OFF = TILE_BYTES;        // K ring; slot 0 stages O at the end
   static constexpr int V_OFF = K_OFF + NST * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + NST * TILE_BYTES;
   // barrier indices
-  static constexpr int B_Q = 0;
+  static constexpr int B_Q = 0;                   // Q tile landed
   static constexpr int B_KFULL = 1;
   static constexpr int B_KEMPTY = B_KFULL + NST;
   static constexpr int B_VFULL = B_KEMPTY + NST;
   static constexpr int B_VEMPTY = B_VFULL + NST;
-  static constexpr int B_SFULL = B_VEMPTY + NST;
-  static constexpr int B_SFREE = B_SFULL + 2;
-  static constexpr int B_PFULL = B_SFREE + 2;
-  static constexpr int B_ODONE = B_PFULL + 2;
-  static constexpr int B_DRAIN = B_ODONE + 1;
-  static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int SMEM_BYTES = BAR_OFF + NBAR * 8 + 16 + 1024;  // + slot/flag + alignment slack
-  // tensor-memory columns (512 allocated): two S buffers, O, two P buffers
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P0 = 384, TM_P1 = 448;
+  static constexpr int B_SFULL = B_VEMPTY + NST;  // S_j in TMEM
+  static constexpr int B_SFREE = B_SFULL + 1;     // S_j read by both halves (256 arrivals)
+  static constexpr int B_PFULL = B_SFREE + 1;     // [buffer][half]: P half in TMEM (128 arrivals)
+  static constexpr int B_ODONE = B_PFULL + 4;     // [half][j parity]: P_j V_j of a half accumulated
+  static constexpr int B_DRAIN = B_ODONE + 4;     // S issuer's MMAs all complete
+  static constexpr int B_DRAIN2 = B_DRAIN + 1;    // P.V issuer's MMAs all complete
+  static constexpr int NBAR = B_DRAIN2 + 1;
+  static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + flags, alignment slack
+  // tensor-memory columns (512 allocated): S, one O accumulator per half, P[buffer][half]
+  static constexpr uint32_t TM_S = 0, TM_O0 = 128, TM_O1 = 128 + D, TM_P = 128 + 2 * D;
   static constexpr uint32_t TM_COLS = 512;
+  static_assert(NBAR * 8 + 8 <= 512, "barrier area");
+  static_assert(TM_P + 128 <= TM_COLS, "tensor memory");
 };
 
 // sites recorded with a timeout (bits 8.. of the error word)
@@ -82,8 +93,39 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Byte address of the 16-byte chunk `chunk` (8 bf16) of row `row` in a
+// 128-row tile stored as 64-column blocks with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t base, int row, int chunk) {
+  return base + (chunk >> 3) * (128 * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// Loads of one ring (K or V) by one producer thread; on an abort it waits
+// for every copy it issued before returning.
+template <int D>
+__device__ __forceinline__ void produce_ring(const CUtensorMap* map, uint32_t ring_base,
+                                             uint32_t full0, uint32_t empty0, int n_kt, int bh,
+                                             const WaitCtl& wc, uint32_t site) {
+  using C = Cfg<D>;
+  int issued = 0;
+  for (int j = 0; j < n_kt; ++j) {
+    const int st = j % C::NST;
+    if (j >= C::NST && !mbar_wait(empty0 + 8u * st, ((j / C::NST) & 1) ^ 1, wc, site)) break;
+    const uint32_t dst = ring_base + st * C::TILE_BYTES;
+    mbar_arrive_expect_tx(full0 + 8u * st, C::TILE_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_3d(dst + kb * C::BLOCK_BYTES, map, full0 + 8u * st, kb * 64, j * BN, bh);
+    ++issued;
+  }
+  if (*wc.abort_flag) {
+    for (int st = 0; st < C::NST && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / C::NST) * C::NST;  // last j with j % NST == st
+      mbar_wait_drain(full0 + 8u * st, (last / C::NST) & 1, kDrainLimitNs);
+    }
+  }
+}
+
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
@@ -97,9 +139,12 @@ __global__ void __launch_bounds__(256, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int n_qt = gridDim.y;
-  const int qt = CAUSAL ? (n_qt - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+  // 1-D grid, query tiles of one (b, h) adjacent so that the CTAs in flight
+  // share their K/V tiles in L2; heaviest tile of each head first (causal)
+  const int n_qt = (S + BM - 1) / BM;
+  const int bh = static_cast<int>(blockIdx.x / n_qt);
+  const int qi = static_cast<int>(blockIdx.x % n_qt);
+  const int qt = CAUSAL ? (n_qt - 1 - qi) : qi;
   const int q0 = qt * BM;
   const int n_kt = CAUSAL ? (qt + 1) : (S + BN - 1) / BN;
 
@@ -116,13 +161,14 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(bar(C::B_VFULL + s), 1);
       mbar_init(bar(C::B_VEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_SFREE + s), 128);
-      mbar_init(bar(C::B_PFULL + s), 128);
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_SFREE), kSoftmaxThreads);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(C::B_PFULL + i), kSoftmaxThreads / 2);
+      mbar_init(bar(C::B_ODONE + i), 1);
     }
-    mbar_init(bar(C::B_ODONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_DRAIN2), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -137,192 +183,210 @@ __global__ void __launch_bounds__(256, 1)
   const WaitCtl wc{wait_limit_ns, &g_err_prefill_bf16, abort_flag};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
       const uint32_t sQ = sbase + C::Q_OFF;
       mbar_arrive_expect_tx(bar(C::B_Q), C::TILE_BYTES);
       for (int kb = 0; kb < C::KB; ++kb)
         tma_load_3d(sQ + kb * C::BLOCK_BYTES, &tmQ, bar(C::B_Q), kb * 64, q0, bh);
-      int nk = 0, nv = 0;  // loads issued
-      for (int j = 0; j < n_kt; ++j) {
-        const int st = j % C::NST;
-        const uint32_t ph = (j / C::NST) & 1;
-        if (j >= C::NST && !mbar_wait(bar(C::B_KEMPTY + st), ph ^ 1, wc, SITE_PROD_KEMPTY)) break;
-        const uint32_t sK = sbase + C::K_OFF + st * C::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(sK + kb * C::BLOCK_BYTES, &tmK, bar(C::B_KFULL + st), kb * 64, j * BN, bh);
-        ++nk;
-        if (j >= C::NST && !mbar_wait(bar(C::B_VEMPTY + st), ph ^ 1, wc, SITE_PROD_VEMPTY)) break;
-        const uint32_t sV = sbase + C::V_OFF + st * C::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(sV + kb * C::BLOCK_BYTES, &tmV, bar(C::B_VFULL + st), kb * 64, j * BN, bh);
-        ++nv;
-      }
-      if (*abort_flag) {
-        // let every copy still in flight land before the CTA can exit
-        mbar_wait_drain(bar(C::B_Q), 0, kDrainLimitNs);
-        for (int st = 0; st < C::NST; ++st) {
-          for (int which = 0; which < 2; ++which) {
-            const int n = which ? nv : nk;
-            if (st >= n) continue;                                // nothing loaded on this stage
-            const int last = st + ((n - 1 - st) / C::NST) * C::NST;  // last j < n with j % NST == st
-            mbar_wait_drain(bar((which ? C::B_VFULL : C::B_KFULL) + st), (last / C::NST) & 1,
-                            kDrainLimitNs);
-          }
-        }
-      }
+      produce_ring<D>(&tmK, sbase + C::K_OFF, bar(C::B_KFULL), bar(C::B_KEMPTY), n_kt, bh, wc,
+                      SITE_PROD_KEMPTY);
+      if (*abort_flag) mbar_wait_drain(bar(C::B_Q), 0, kDrainLimitNs);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ V producer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      const uint32_t sQ = sbase + C::Q_OFF;
-      auto issue_pv = [&](int jj) -> bool {
-        const int st = jj % C::NST;
-        const int pb = jj & 1;
-        if (!mbar_wait(bar(C::B_PFULL + pb), (jj >> 1) & 1, wc, SITE_MMA_PFULL)) return false;
-        if (!mbar_wait(bar(C::B_VFULL + st), (jj / C::NST) & 1, wc, SITE_MMA_VFULL)) return false;
-        tc_fence_after();
-        const uint32_t sV = sbase + C::V_OFF + st * C::TILE_BYTES;
-        const uint32_t tP = tmem + (pb ? C::TM_P1 : C::TM_P0);
+      prefetch_tensormap(&tmV);
+      produce_ring<D>(&tmV, sbase + C::V_OFF, bar(C::B_VFULL), bar(C::B_VEMPTY), n_kt, bh, wc,
+                      SITE_PROD_VEMPTY);
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads feed the tensor pipe: warp 1 issues S_j = Q K_j^T, warp 3
+    // issues the two halves of P_j V_j.  Each thread's barrier waits and
+    // commits then overlap the other's MMAs.  The two streams only meet
+    // through barriers: S_{j+1} waits until both halves have read S_j, a half
+    // of P_j V_j waits for that half of P_j.
+    if (lane == 0) {
+      const bool s_issuer = (warp == 1);
+      bool ok = true;
+      if (s_issuer) {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, BN, false);
+        const uint64_t qdesc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);  // K-major, LBO unused
+        const uint64_t kdesc0 = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
+        ok = mbar_wait(bar(C::B_Q), 0, wc, SITE_MMA_Q);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int st = j % C::NST;
+          ok = mbar_wait(bar(C::B_KFULL + st), (j / C::NST) & 1, wc, SITE_MMA_KFULL);
+          // the single S buffer is free once both halves have read S_{j-1}
+          if (ok && j >= 1) ok = mbar_wait(bar(C::B_SFREE), (j - 1) & 1, wc, SITE_MMA_SFREE);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kdesc = kdesc0 + ((st * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          // V tile is MN-major for this product: 16 keys = 16 rows of 128 B = 2048 B
-          const uint64_t bdesc = smem_desc_sw128(sV + k * 2048, C::BLOCK_BYTES, 1024);
-          umma_ts(tmem + C::TM_O, tP + k * 8, bdesc, idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < D / 16; ++k) {
+            // 16 columns = 32 bytes within a 128-byte row, 64 columns per block
+            const uint32_t off = ((k >> 2) * C::BLOCK_BYTES + (k & 3) * 32) >> 4;
+            umma_ss(tmem + C::TM_S, qdesc0 + off, kdesc + off, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::B_SFULL));
+          umma_commit(bar(C::B_KEMPTY + st));
         }
-        umma_commit(bar(C::B_VEMPTY + st));
-        umma_commit(bar(C::B_ODONE));
-        return true;
-      };
-      bool ok = mbar_wait(bar(C::B_Q), 0, wc, SITE_MMA_Q);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const int st = j % C::NST;
-        const int sb = j & 1;
-        if (!mbar_wait(bar(C::B_KFULL + st), (j / C::NST) & 1, wc, SITE_MMA_KFULL)) {
-          ok = false;
-          break;
-        }
-        if (j >= 2 && !mbar_wait(bar(C::B_SFREE + sb), ((j >> 1) & 1) ^ 1, wc, SITE_MMA_SFREE)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sK = sbase + C::K_OFF + st * C::TILE_BYTES;
-        const uint32_t tS = tmem + (sb ? C::TM_S1 : C::TM_S0);
+      } else {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
+        // V tile MN-major for this product: LBO = next 64 columns, 16 keys = 2048 bytes
+        const uint64_t vdesc0 = smem_desc_sw128(sbase + C::V_OFF, C::BLOCK_BYTES, 1024);
+        for (int j = 0; ok && j < n_kt; ++j) {
+          const int st = j % C::NST;
+          const int pb = j & 1;
+          ok = mbar_wait(bar(C::B_VFULL + st), (j / C::NST) & 1, wc, SITE_MMA_VFULL);
+          const uint64_t vdesc = vdesc0 + ((st * C::TILE_BYTES) >> 4);
+          for (int h = 0; ok && h < 2; ++h) {
+            ok = mbar_wait(bar(C::B_PFULL + pb * 2 + h), (j >> 1) & 1, wc, SITE_MMA_PFULL);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tP = tmem + C::TM_P + pb * 64 + h * 32;
+            const uint32_t tO = tmem + (h ? C::TM_O1 : C::TM_O0);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::BLOCK_BYTES + (k & 3) * 32;
-          const uint64_t adesc = smem_desc_sw128(sQ + off, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(sK + off, 16, 1024);
-          umma_ss(tS, adesc, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)  // keys 64h + 16k .. +15
+              umma_ts(tO, tP + k * 8, vdesc + (((4 * h + k) * 2048) >> 4), idesc,
+                      (j > 0 || k > 0) ? 1u : 0u);
+            umma_commit(bar(C::B_ODONE + h * 2 + (j & 1)));
+          }
+          if (ok) umma_commit(bar(C::B_VEMPTY + st));
         }
-        umma_commit(bar(C::B_SFULL + sb));
-        umma_commit(bar(C::B_KEMPTY + st));
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
-      if (ok) issue_pv(n_kt - 1);
       // every MMA this thread issued completes before tensor memory is freed
-      umma_commit(bar(C::B_DRAIN));
-      mbar_wait_drain(bar(C::B_DRAIN), 0, kDrainLimitNs);
+      const uint32_t drain = bar(s_issuer ? C::B_DRAIN : C::B_DRAIN2);
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, kDrainLimitNs);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int wq = warp - 4;  // TMEM lane quarter this warp may access
+    // Two independent warpgroups: half h takes key columns 64h..64h+63 of
+    // every tile with its own running maximum m_h, running sums and its own
+    // output accumulator O_h = sum over its keys of P V.  The halves never
+    // wait for each other inside the loop; the epilogue merges them with the
+    // log-sum-exp rule  O = (O_0 2^m_0 + O_1 2^m_1) / (l_0 2^m_0 + l_1 2^m_1).
+    const int h = (warp - 4) >> 2;
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
     const int q = q0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    float m_run = -INFINITY;  // reference maximum, log2 units
-    float l_run = 0.f;        // sum of the fp32 weights: gives the log-sum-exp
-    float lp_run = 0.f;       // sum of the bf16-rounded weights: normalises O
-    bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + sb), (j >> 1) & 1, wc, SITE_SM_SFULL));
-      if (!ok) break;
+    const uint32_t tO_own = tmem + lane_base + (h ? C::TM_O1 : C::TM_O0);
+    const uint32_t odone = bar(C::B_ODONE + h * 2);
+    float m_run = -INFINITY;  // this half's reference maximum, log2 units
+    float l_run = 0.f;        // sum of fp32 weights: gives the log-sum-exp
+    float lp_run = 0.f;       // sum of bf16-rounded weights: normalises O
+    bool failed = false;
+    for (int j = 0; j < n_kt && !failed; ++j) {
+      const int pb = j & 1;
+      uint32_t s[64];
+      const int key0 = j * BN + h * 64;
+      failed = !__all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL), j & 1, wc, SITE_SM_SFULL));
+      if (failed) break;
       tc_fence_after();
-      uint32_t s[128];
-      {
-        uint32_t (&lo)[64] = *reinterpret_cast<uint32_t(*)[64]>(&s[0]);
-        uint32_t (&hi)[64] = *reinterpret_cast<uint32_t(*)[64]>(&s[64]);
-        const uint32_t tS = tmem + lane_base + (sb ? C::TM_S1 : C::TM_S0);
-        tmem_ld_32x32b_x64(tS, lo);
-        tmem_ld_32x32b_x64(tS + 64, hi);
-      }
+      tmem_ld_32x32b_x64(tmem + lane_base + C::TM_S + h * 64, s);
       tc_fence_before();
-      mbar_arrive(bar(C::B_SFREE + sb));
-
-      const int key0 = j * BN;
-      const bool need_mask = CAUSAL ? (j == n_kt - 1) : (key0 + BN > S);
+      mbar_arrive(bar(C::B_SFREE));
+      const bool need_mask = CAUSAL ? (j == n_kt - 1) : (j * BN + BN > S);
       if (need_mask) {
-        // last key index (within this tile) the row may use
+        // last key index (within this half tile) the row may use
         const int lim = (CAUSAL ? min(q, S - 1) : (S - 1)) - key0;
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i > lim) s[i] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(s[0]);
+      // row maximum over this half: eight independent chains, three-input max
+      float m8[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
+#pragma unroll
+      for (int i = 16; i < 64; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          m8[k] = max3f(m8[k], __uint_as_float(s[i + k]), __uint_as_float(s[i + 8 + k]));
+      const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                             fmaxf(m8[6], m8[7]));
+      // A half-row may be entirely masked on the diagonal tile (all of its
+      // keys lie above the row's own position): it then contributes nothing.
       const float m_new = fmaxf(m_run, mx * c_log2);
       // The reference maximum only moves when the row maximum has grown by
       // more than 8 (log2 units): weights stay <= 256, exact in fp32 and in
       // bf16's exponent range, and O is rescaled far less often.  Softmax is
       // unchanged by the choice of reference, so this is exact arithmetic.
-      const float m_use = (j == 0 || m_new > m_run + 8.0f) ? m_new : m_run;
-      const float neg_m = -m_use;
-      float rs = 0.f, rsp = 0.f;
-      uint32_t p[64];
+      const bool first = (m_run == -INFINITY);
+      const float m_use = (first || m_new > m_run + 8.0f) ? m_new : m_run;
+      // exponent offset; a fully masked half-row (m_use = -inf) gets weights 0
+      const float neg_m = (m_use == -INFINITY) ? 0.0f : -m_use;
+      const float2 c2 = make_float2(c_log2, c_log2);
+      const float2 nm2 = make_float2(neg_m, neg_m);
+      // partial sums: the fp32 weights (for the log-sum-exp) and the
+      // bf16-rounded weights the P.V product uses (to normalise O, so that O
+      // is an exact convex combination of V rows)
+      float2 se[4];
+      float sr[8];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float a = ex2_approx(fmaf(__uint_as_float(s[2 * i]), c_log2, neg_m));
-        const float b = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), c_log2, neg_m));
-        p[i] = pack_bf16x2(a, b);
-        rs += a + b;
-        // O is normalised by the sum of the bf16-rounded weights the P.V
-        // product actually used, so O is an exact convex combination of V rows
-        rsp += __uint_as_float(p[i] << 16) + __uint_as_float(p[i] & 0xffff0000u);
+      for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sr[k] = 0.f;
+      uint32_t p[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                              c2, nm2);
+        float2 e;
+        if (kPolyEvery > 0 && (i + 1) % (kPolyEvery > 0 ? kPolyEvery : 1) == 0) {
+          e = exp2_poly2(x);  // FMA pipe: relieves the special-function unit
+        } else {
+          e.x = ex2_approx(x.x);
+          e.y = ex2_approx(x.y);
+        }
+        p[i] = pack_bf16x2(e.x, e.y);
+        se[i & 3] = add2(se[i & 3], e);
+        sr[(i & 3) * 2] = add_bf16_lo(p[i], sr[(i & 3) * 2]);
+        sr[(i & 3) * 2 + 1] = add_bf16_hi(p[i], sr[(i & 3) * 2 + 1]);
       }
-      {
-        const uint32_t tP = tmem + lane_base + (sb ? C::TM_P1 : C::TM_P0);
-        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[0]);
-        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&p[32]);
-        tmem_st_32x32b_x32(tP, p0);
-        tmem_st_32x32b_x32(tP + 32, p1);
-        tmem_wait_st();
-      }
-      if (j > 0) {
-        // O must hold P_{j-1} V_{j-1} before it is rescaled
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE), (j - 1) & 1, wc, SITE_SM_ODONE));
-        if (!ok) break;
+      se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
+      const float rs = se[0].x + se[0].y;
+      const float rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+      // P_j goes to buffer j % 2: this half's P_{j-2} V_{j-2} must have read
+      // it.  The two O_DONE barriers of a half (even / odd j) each advance
+      // once every other tile and every thread waits on each of their phases
+      // in order, so a parity wait can never see a barrier two phases ahead.
+      if (j >= 2)
+        failed = !__all_sync(0xffffffffu, mbar_wait(odone + 8u * (j & 1), ((j - 2) >> 1) & 1, wc,
+                                                    SITE_SM_ODONE));
+      if (failed) break;
+      tmem_st_32x32b_x32(tmem + lane_base + C::TM_P + pb * 64 + h * 32, p);
+      tmem_wait_st();
+      const bool resc = !first && (m_use != m_run);
+      if (__any_sync(0xffffffffu, resc)) {
+        // O_h must hold P_{j-1} V_{j-1} before it is rescaled.  Tiles that
+        // need no rescale (the common case with the lazy reference maximum)
+        // skip this wait, so P_j V_j queues right behind P_{j-1} V_{j-1}
+        // (same accumulator: executed in issue order).
+        failed = !__all_sync(0xffffffffu, mbar_wait(odone + 8u * ((j - 1) & 1), ((j - 1) >> 1) & 1,
+                                                    wc, SITE_SM_ODONE));
+        if (failed) break;
         tc_fence_after();
-        const bool resc = (m_use != m_run);
-        if (__any_sync(0xffffffffu, resc)) {
-          const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
+        const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            const uint32_t tO = tmem + lane_base + C::TM_O + c * 32;
-            tmem_ld_32x32b_x32(tO, o);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO_own + c * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_32x32b_x32(tO, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(tO_own + c * 32, o);
         }
-        if (resc) {
-          const float alpha = ex2_approx(m_run - m_use);
-          l_run *= alpha;
-          lp_run *= alpha;
-        }
+        tmem_wait_st();
+        l_run *= alpha;
+        lp_run *= alpha;
       }
       l_run += rs;
       lp_run += rsp;
@@ -330,38 +394,61 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_before();
       // failure-detection test mode: the first "P ready" signal is withheld,
       // so the MMA thread's bounded wait for it runs out
-      if (!(inject == 1 && j == 0)) mbar_arrive(bar(C::B_PFULL + sb));
+      if (!(inject == 1 && j == 0)) mbar_arrive(bar(C::B_PFULL + pb * 2 + h));
     }
     // ---------------------------------------------------------- epilogue
-    if (ok)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::B_ODONE), (n_kt - 1) & 1, wc, SITE_SM_OFINAL));
-    const uint32_t sO = sbase + C::Q_OFF;  // Q is no longer read: the last S MMA completed
-    if (ok) {
+    // the last P V of a half done implies all earlier ones (same accumulator, in order)
+    if (!failed)
+      failed = !__all_sync(0xffffffffu, mbar_wait(odone + 8u * ((n_kt - 1) & 1),
+                                                  ((n_kt - 1) >> 1) & 1, wc, SITE_SM_OFINAL));
+    // exchange (m, l, lp) between the halves through the Q tile's smem:
+    // every S product (the only reader of Q) has completed
+    float* xs = reinterpret_cast<float*>(smem + C::Q_OFF);  // [half][3][128]
+    xs[(h * 3 + 0) * BM + row] = m_run;
+    xs[(h * 3 + 1) * BM + row] = l_run;
+    xs[(h * 3 + 2) * BM + row] = lp_run;
+    failed = bar_red_or(1, kSoftmaxThreads, failed);
+    // O is staged in K ring slot 0: every S product (the only reader of K) has completed
+    const uint32_t sO = sbase + C::K_OFF;
+    if (!failed) {
+      const float m_oth = xs[((h ^ 1) * 3 + 0) * BM + row];
+      const float m0 = h ? m_oth : m_run, m1 = h ? m_run : m_oth;
+      const float l0 = h ? xs[(0 * 3 + 1) * BM + row] : l_run;
+      const float l1 = h ? l_run : xs[(1 * 3 + 1) * BM + row];
+      const float lp0 = h ? xs[(0 * 3 + 2) * BM + row] : lp_run;
+      const float lp1 = h ? lp_run : xs[(1 * 3 + 2) * BM + row];
+      const float M = fmaxf(m0, m1);
+      const float w0 = (m0 == -INFINITY) ? 0.f : ex2_approx(m0 - M);
+      const float w1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - M);
+      const float l_tot = l0 * w0 + l1 * w1;
+      const float inv_lp = 1.0f / (lp0 * w0 + lp1 * w1);
+      const float s0 = w0 * inv_lp, s1 = w1 * inv_lp;
       tc_fence_after();
-      const float inv_l = 1.0f / lp_run;
+      // this half writes output columns [h D/2, (h+1) D/2) from both accumulators
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + C::TM_O + c * 32, o);
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = h * (D / 2) + c * 32;
+        uint32_t o0[32], o1[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + C::TM_O0 + col, o0);
+        tmem_ld_32x32b_x32(tmem + lane_base + C::TM_O1 + col, o1);
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = c * 4 + c4;  // 16-byte chunk of this row
-          const int kb = chunk >> 3, cc = chunk & 7;
-          const uint32_t addr = sO + kb * C::BLOCK_BYTES + row * 128 + ((cc ^ (row & 7)) << 4);
-          st_shared_v4(addr, w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+        for (int i = 0; i < 16; ++i) {
+          const float a = __uint_as_float(o0[2 * i]) * s0 + __uint_as_float(o1[2 * i]) * s1;
+          const float b = __uint_as_float(o0[2 * i + 1]) * s0 + __uint_as_float(o1[2 * i + 1]) * s1;
+          w[i] = pack_bf16x2(a, b);
         }
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          st_shared_v4(sw128_chunk(sO, row, col / 8 + c4), w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2],
+                       w[4 * c4 + 3]);
       }
-      if (lse != nullptr && q < S)
-        lse[static_cast<size_t>(bh) * S + q] = (m_run + __log2f(l_run)) * kLn2;
+      if (h == 0 && lse != nullptr && q < S)
+        lse[static_cast<size_t>(bh) * S + q] = (M + __log2f(l_tot)) * kLn2;
       fence_proxy_async_smem();
     }
-    named_barrier_sync(1, 128);
-    if (threadIdx.x == 128 && !*abort_flag) {
+    named_barrier_sync(1, kSoftmaxThreads);
+    if (threadIdx.x == 128 && !failed) {
       for (int kb = 0; kb < C::KB; ++kb) tma_store_3d(&tmO, sO + kb * C::BLOCK_BYTES, kb * 64, q0, bh);
       tma_store_commit();
       tma_store_wait_all();
@@ -418,8 +505,8 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   auto kern = prefill_bf16_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(BH, (S + BM - 1) / BM);
-  kern<<<grid, 256, smem, stream>>>(mq, mk, mv, mo, lse, S, c_log2, wait_limit_ns, inject);
+  dim3 grid(static_cast<unsigned>(BH) * ((S + BM - 1) / BM));
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mo, lse, S, c_log2, wait_limit_ns, inject);
   return cudaGetLastError();
 }
 
