@@ -15,11 +15,11 @@
 // One CTA computes one 128-row query tile of one (batch, head), 384 threads:
 //   warp 0       TMA producer for Q (once) and the K ring
 //   warp 2       TMA producer for the V ring
-//   warp 1       TMEM allocation; one thread issues S_j = Q K_j^T (both
-//                operands from smem)
-//   warp 3       one thread issues O_h += P_j,h V_j,h for the two key halves
-//                h (A = P from TMEM, B = V from smem, MN-major); two issuers
-//                keep the tensor pipe fed while each does its bookkeeping
+//   warps 1, 12  TMEM allocation (warp 1); one thread each issues the key
+//                half h = 0 / 1 of S_j = Q K_j^T (both operands from smem)
+//   warps 3, 13  one thread each issues O_h += P_j,h V_j,h for h = 0 / 1
+//                (A = P from TMEM, B = V from smem, MN-major); four issuers
+//                keep the tensor pipe fed, none waiting on another's inputs
 //   warps 4..11  softmax, two independent warpgroups: half h owns key
 //                columns 64h..64h+63 of every tile, with its own running
 //                maximum, sums and output accumulator O_h in TMEM; it writes
@@ -47,7 +47,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // one pair of exponentials in kPolyEvery goes to the FMA-pipe polynomial (0: none)
 constexpr int kPolyEvery = 0;
 constexpr int kSoftmaxThreads = 256;  // two warpgroups, warps 4..11
-constexpr int kThreads = 128 + kSoftmaxThreads;
+constexpr int kThreads = 128 + kSoftmaxThreads + 64;  // + warps 12, 13: issuers of half 1
 
 template <int D>
 struct Cfg {
@@ -65,24 +65,25 @@ struct Cfg {
   static constexpr int B_KEMPTY = B_KFULL + NST;
   static constexpr int B_VFULL = B_KEMPTY + NST;
   static constexpr int B_VEMPTY = B_VFULL + NST;
-  static constexpr int B_SFULL = B_VEMPTY + NST;  // S_j in TMEM
-  static constexpr int B_SFREE = B_SFULL + 1;     // S_j read by both halves (256 arrivals)
-  static constexpr int B_PFULL = B_SFREE + 1;     // [buffer][half]: P half in TMEM (128 arrivals)
+  static constexpr int B_SFULL = B_VEMPTY + NST;  // [buffer][half]: a half of S_j in TMEM
+  static constexpr int B_PFULL = B_SFULL + 4;     // [buffer][half]: P half in TMEM (128 arrivals)
   static constexpr int B_ODONE = B_PFULL + 4;     // [half][j parity]: P_j V_j of a half accumulated
-  static constexpr int B_DRAIN = B_ODONE + 4;     // S issuer's MMAs all complete
-  static constexpr int B_DRAIN2 = B_DRAIN + 1;    // P.V issuer's MMAs all complete
-  static constexpr int NBAR = B_DRAIN2 + 1;
+  static constexpr int B_DRAIN = B_ODONE + 4;     // [issuer]: all MMAs of an issuer complete
+  static constexpr int NBAR = B_DRAIN + 4;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + flags, alignment slack
-  // tensor-memory columns (512 allocated): S, one O accumulator per half, P[buffer][half]
-  static constexpr uint32_t TM_S = 0, TM_O0 = 128, TM_O1 = 128 + D, TM_P = 128 + 2 * D;
+  // tensor-memory columns (512 allocated): two S buffers, one O accumulator
+  // per half.  P_j of half h (64 keys as bf16 pairs = 32 columns) is written
+  // over the first 32 of that half's 64 columns of S buffer j % 2, after the
+  // thread owning the row has read them.
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(NBAR * 8 + 8 <= 512, "barrier area");
-  static_assert(TM_P + 128 <= TM_COLS, "tensor memory");
+  static_assert(TM_O1 + D <= TM_COLS, "tensor memory");
 };
 
 // sites recorded with a timeout (bits 8.. of the error word)
 enum : uint32_t {
-  SITE_PROD_KEMPTY = 1, SITE_PROD_VEMPTY, SITE_MMA_Q, SITE_MMA_KFULL, SITE_MMA_SFREE,
+  SITE_PROD_KEMPTY = 1, SITE_PROD_VEMPTY, SITE_MMA_Q, SITE_MMA_KFULL, SITE_MMA_SFREE /* S buffer */,
   SITE_MMA_PFULL, SITE_MMA_VFULL, SITE_SM_SFULL, SITE_SM_ODONE, SITE_SM_OFINAL
 };
 
@@ -157,18 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_Q), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 2);  // released by the two S issuers
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 2);  // released by the two P.V issuers
     }
-    mbar_init(bar(C::B_SFULL), 1);
-    mbar_init(bar(C::B_SFREE), kSoftmaxThreads);
     for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(C::B_SFULL + i), 1);
       mbar_init(bar(C::B_PFULL + i), kSoftmaxThreads / 2);
       mbar_init(bar(C::B_ODONE + i), 1);
     }
-    mbar_init(bar(C::B_DRAIN), 1);
-    mbar_init(bar(C::B_DRAIN2), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -204,69 +203,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                       SITE_PROD_VEMPTY);
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 3) {
+  } else if (warp == 1 || warp == 3 || warp == 12 || warp == 13) {
     // ------------------------------------------------------------ MMA issuers
-    // Two threads feed the tensor pipe: warp 1 issues S_j = Q K_j^T, warp 3
-    // issues the two halves of P_j V_j.  Each thread's barrier waits and
-    // commits then overlap the other's MMAs.  The two streams only meet
-    // through barriers: S_{j+1} waits until both halves have read S_j, a half
-    // of P_j V_j waits for that half of P_j.
+    // Four threads feed the tensor pipe, one per stream: S_j,h = Q K_j,h^T for
+    // key half h = 0 (warp 1) and h = 1 (warp 12), and O_h += P_j,h V_j,h for
+    // h = 0 (warp 3) and h = 1 (warp 13).  Each stream waits only for its own
+    // inputs, so a lagging half never holds up the other, and one thread's
+    // barrier bookkeeping overlaps the others' MMAs.  A half of S_j goes to
+    // buffer j % 2 once that half's P_{j-2} V_{j-2} (which read P_{j-2} from
+    // there) has completed; a half of P_j V_j waits for that half of P_j.
     if (lane == 0) {
-      const bool s_issuer = (warp == 1);
+      const bool s_issuer = (warp == 1 || warp == 12);
+      const int h = (warp >= 12) ? 1 : 0;
       bool ok = true;
       if (s_issuer) {
-        constexpr uint32_t idesc = idesc_bf16_f32(128, BN, false);
+        constexpr uint32_t idesc = idesc_bf16_f32(128, BN / 2, false);
         const uint64_t qdesc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);  // K-major, LBO unused
-        const uint64_t kdesc0 = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
+        // rows 64h.. of each K tile: 64 rows x 128 B further into each block
+        const uint64_t kdesc0 = smem_desc_sw128(sbase + C::K_OFF + h * 64 * 128, 16, 1024);
         ok = mbar_wait(bar(C::B_Q), 0, wc, SITE_MMA_Q);
         for (int j = 0; ok && j < n_kt; ++j) {
           const int st = j % C::NST;
+          const int pb = j & 1;
           ok = mbar_wait(bar(C::B_KFULL + st), (j / C::NST) & 1, wc, SITE_MMA_KFULL);
-          // the single S buffer is free once both halves have read S_{j-1}
-          if (ok && j >= 1) ok = mbar_wait(bar(C::B_SFREE), (j - 1) & 1, wc, SITE_MMA_SFREE);
+          // buffer j % 2 of this half held P_{j-2}: P_{j-2} V_{j-2} must be done
+          if (ok && j >= 2)
+            ok = mbar_wait(bar(C::B_ODONE + h * 2 + pb), ((j - 2) >> 1) & 1, wc, SITE_MMA_SFREE);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t tS = tmem + (pb ? C::TM_S1 : C::TM_S0) + h * 64;
           const uint64_t kdesc = kdesc0 + ((st * C::TILE_BYTES) >> 4);
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            // 16 columns = 32 bytes within a 128-byte row, 64 columns per block
-            const uint32_t off = ((k >> 2) * C::BLOCK_BYTES + (k & 3) * 32) >> 4;
-            umma_ss(tmem + C::TM_S, qdesc0 + off, kdesc + off, idesc, k > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::B_SFULL));
+          // k steps of 16 columns: 32 bytes within a 128-byte row, 64 columns per block
+          if constexpr (D == 128)
+            umma_ss_kmajor_x8(tS, qdesc0, kdesc, idesc, 0u);
+          else
+            umma_ss_kmajor_x4(tS, qdesc0, kdesc, idesc, 0u);
+          umma_commit(bar(C::B_SFULL + pb * 2 + h));
           umma_commit(bar(C::B_KEMPTY + st));
         }
       } else {
         constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
-        // V tile MN-major for this product: LBO = next 64 columns, 16 keys = 2048 bytes
-        const uint64_t vdesc0 = smem_desc_sw128(sbase + C::V_OFF, C::BLOCK_BYTES, 1024);
+        // V tile MN-major for this product: LBO = next 64 columns, 16 keys = 2048 bytes;
+        // this half's keys start 64 rows into the tile
+        const uint64_t vdesc0 = smem_desc_sw128(sbase + C::V_OFF + h * 64 * 128, C::BLOCK_BYTES, 1024);
+        const uint32_t tO = tmem + (h ? C::TM_O1 : C::TM_O0);
         for (int j = 0; ok && j < n_kt; ++j) {
           const int st = j % C::NST;
           const int pb = j & 1;
           ok = mbar_wait(bar(C::B_VFULL + st), (j / C::NST) & 1, wc, SITE_MMA_VFULL);
+          if (ok) ok = mbar_wait(bar(C::B_PFULL + pb * 2 + h), (j >> 1) & 1, wc, SITE_MMA_PFULL);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tP = tmem + (pb ? C::TM_S1 : C::TM_S0) + h * 64;
           const uint64_t vdesc = vdesc0 + ((st * C::TILE_BYTES) >> 4);
-          for (int h = 0; ok && h < 2; ++h) {
-            ok = mbar_wait(bar(C::B_PFULL + pb * 2 + h), (j >> 1) & 1, wc, SITE_MMA_PFULL);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t tP = tmem + C::TM_P + pb * 64 + h * 32;
-            const uint32_t tO = tmem + (h ? C::TM_O1 : C::TM_O0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // keys 64h + 16k .. +15
-              umma_ts(tO, tP + k * 8, vdesc + (((4 * h + k) * 2048) >> 4), idesc,
-                      (j > 0 || k > 0) ? 1u : 0u);
-            umma_commit(bar(C::B_ODONE + h * 2 + (j & 1)));
-          }
-          if (ok) umma_commit(bar(C::B_VEMPTY + st));
+          // keys 64h + 16k .. +15 for k = 0..3: 8 TMEM columns of P, 2048 B of V each
+          umma_ts_mnmajor_x4(tO, tP, vdesc, idesc, j > 0 ? 1u : 0u);
+          umma_commit(bar(C::B_ODONE + h * 2 + pb));
+          umma_commit(bar(C::B_VEMPTY + st));
         }
       }
       // every MMA this thread issued completes before tensor memory is freed
-      const uint32_t drain = bar(s_issuer ? C::B_DRAIN : C::B_DRAIN2);
+      const uint32_t drain = bar(C::B_DRAIN + (s_issuer ? 0 : 2) + h);
       umma_commit(drain);
       mbar_wait_drain(drain, 0, kDrainLimitNs);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / epilogue
     // Two independent warpgroups: half h takes key columns 64h..64h+63 of
     // every tile with its own running maximum m_h, running sums and its own
@@ -288,12 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pb = j & 1;
       uint32_t s[64];
       const int key0 = j * BN + h * 64;
-      failed = !__all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL), j & 1, wc, SITE_SM_SFULL));
+      const uint32_t tS = tmem + lane_base + (pb ? C::TM_S1 : C::TM_S0) + h * 64;
+      failed = !__all_sync(0xffffffffu,
+                           mbar_wait(bar(C::B_SFULL + pb * 2 + h), (j >> 1) & 1, wc, SITE_SM_SFULL));
       if (failed) break;
       tc_fence_after();
-      tmem_ld_32x32b_x64(tmem + lane_base + C::TM_S + h * 64, s);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_SFREE));
+      tmem_ld_32x32b_x64(tS, s);
       const bool need_mask = CAUSAL ? (j == n_kt - 1) : (j * BN + BN > S);
       if (need_mask) {
         // last key index (within this half tile) the row may use
@@ -355,22 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
       const float rs = se[0].x + se[0].y;
       const float rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
-      // P_j goes to buffer j % 2: this half's P_{j-2} V_{j-2} must have read
-      // it.  The two O_DONE barriers of a half (even / odd j) each advance
-      // once every other tile and every thread waits on each of their phases
-      // in order, so a parity wait can never see a barrier two phases ahead.
-      if (j >= 2)
-        failed = !__all_sync(0xffffffffu, mbar_wait(odone + 8u * (j & 1), ((j - 2) >> 1) & 1, wc,
-                                                    SITE_SM_ODONE));
-      if (failed) break;
-      tmem_st_32x32b_x32(tmem + lane_base + C::TM_P + pb * 64 + h * 32, p);
+      // P_j of this half goes over the S columns this thread has just read
+      tmem_st_32x32b_x32(tS, p);
       tmem_wait_st();
       const bool resc = !first && (m_use != m_run);
       if (__any_sync(0xffffffffu, resc)) {
         // O_h must hold P_{j-1} V_{j-1} before it is rescaled.  Tiles that
         // need no rescale (the common case with the lazy reference maximum)
         // skip this wait, so P_j V_j queues right behind P_{j-1} V_{j-1}
-        // (same accumulator: executed in issue order).
+        // (same accumulator: executed in issue order).  The parity wait is
+        // exact: the barrier's previous phase (P_{j-3} V_{j-3}) completed
+        // before this half of S_{j-1} was issued, and its next one needs P_{j+1}.
         failed = !__all_sync(0xffffffffu, mbar_wait(odone + 8u * ((j - 1) & 1), ((j - 1) >> 1) & 1,
                                                     wc, SITE_SM_ODONE));
         if (failed) break;
@@ -401,14 +398,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed)
       failed = !__all_sync(0xffffffffu, mbar_wait(odone + 8u * ((n_kt - 1) & 1),
                                                   ((n_kt - 1) >> 1) & 1, wc, SITE_SM_OFINAL));
-    // exchange (m, l, lp) between the halves through the Q tile's smem:
-    // every S product (the only reader of Q) has completed
-    float* xs = reinterpret_cast<float*>(smem + C::Q_OFF);  // [half][3][128]
-    xs[(h * 3 + 0) * BM + row] = m_run;
-    xs[(h * 3 + 1) * BM + row] = l_run;
-    xs[(h * 3 + 2) * BM + row] = lp_run;
+    // Once both halves are past this barrier, both have consumed their last
+    // S (so no MMA reads Q or K any more) and both last P V are complete.
     failed = bar_red_or(1, kSoftmaxThreads, failed);
-    // O is staged in K ring slot 0: every S product (the only reader of K) has completed
+    // exchange (m, l, lp) between the halves through the Q tile's smem
+    float* xs = reinterpret_cast<float*>(smem + C::Q_OFF);  // [half][3][128]
+    if (!failed) {
+      xs[(h * 3 + 0) * BM + row] = m_run;
+      xs[(h * 3 + 1) * BM + row] = l_run;
+      xs[(h * 3 + 2) * BM + row] = lp_run;
+    }
+    named_barrier_sync(1, kSoftmaxThreads);
+    // O is staged in K ring slot 0
     const uint32_t sO = sbase + C::K_OFF;
     if (!failed) {
       const float m_oth = xs[((h ^ 1) * 3 + 0) * BM + row];

@@ -231,6 +231,95 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Groups of MMAs issued from one asm block: the descriptors of the k steps
+// are the base plus constant offsets (in 16-byte units), so issuing a group
+// costs a handful of instructions.  The first MMA accumulates into D only
+// when acc_first != 0; the rest always accumulate.
+// 8 MMAs D += A B^T over K = 128, A and B K-major 128-byte-swizzled smem tiles (64-column blocks)
+__device__ __forceinline__ void umma_ss_kmajor_x8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc_first) {
+  asm volatile("{\n\t"
+               ".reg .pred pf, pt;\n\t"
+               ".reg .b64 b;\n\t"
+               ".reg .b64 a;\n\t"
+               "setp.ne.b32 pf, %4, 0;\n\t"
+               "setp.eq.b32 pt, %4, %4;\n\t"
+               "add.s64 b, %2, 0;\n\t"
+               "add.s64 a, %1, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pf;\n\t"
+               "add.s64 b, %2, 2;\n\t"
+               "add.s64 a, %1, 2;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 4;\n\t"
+               "add.s64 a, %1, 4;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 6;\n\t"
+               "add.s64 a, %1, 6;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 1024;\n\t"
+               "add.s64 a, %1, 1024;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 1026;\n\t"
+               "add.s64 a, %1, 1026;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 1028;\n\t"
+               "add.s64 a, %1, 1028;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 1030;\n\t"
+               "add.s64 a, %1, 1030;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "}"
+               :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc_first) : "memory");
+}
+
+// 4 MMAs D += A B^T over K = 64, A and B K-major 128-byte-swizzled smem tiles
+__device__ __forceinline__ void umma_ss_kmajor_x4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc_first) {
+  asm volatile("{\n\t"
+               ".reg .pred pf, pt;\n\t"
+               ".reg .b64 b;\n\t"
+               ".reg .b64 a;\n\t"
+               "setp.ne.b32 pf, %4, 0;\n\t"
+               "setp.eq.b32 pt, %4, %4;\n\t"
+               "add.s64 b, %2, 0;\n\t"
+               "add.s64 a, %1, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pf;\n\t"
+               "add.s64 b, %2, 2;\n\t"
+               "add.s64 a, %1, 2;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 4;\n\t"
+               "add.s64 a, %1, 4;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 b, %2, 6;\n\t"
+               "add.s64 a, %1, 6;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "}"
+               :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc_first) : "memory");
+}
+
+// 4 MMAs D += A B over K = 64: A from TMEM (8 columns per 16 k), B MN-major smem (16 rows of 128 B per 16 k)
+__device__ __forceinline__ void umma_ts_mnmajor_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t acc_first) {
+  asm volatile("{\n\t"
+               ".reg .pred pf, pt;\n\t"
+               ".reg .b64 b;\n\t"
+               ".reg .b32 a;\n\t"
+               "setp.ne.b32 pf, %4, 0;\n\t"
+               "setp.eq.b32 pt, %4, %4;\n\t"
+               "add.s64 b, %2, 0;\n\t"
+               "add.u32 a, %1, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pf;\n\t"
+               "add.s64 b, %2, 128;\n\t"
+               "add.u32 a, %1, 8;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+               "add.s64 b, %2, 256;\n\t"
+               "add.u32 a, %1, 16;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+               "add.s64 b, %2, 384;\n\t"
+               "add.u32 a, %1, 24;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+               "}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc_first) : "memory");
+}
+
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
