@@ -43,23 +43,28 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
 # named workload, valid only while the kernel source hashes to the recorded value.
 TRAFFIC = {
-    "prefill": {"file": "causal_head_attention_mha_gb300/csrc/prefill_bf16.cu", "sha256": None,
-                "bytes_per_launch": None},
-    "decode": {"file": "causal_head_attention_mha_gb300/csrc/decode.cu", "sha256": None,
-               "bytes_per_launch": None},
+    # profiles/prefill_bf16_d128_causal_b4h32s4096.md
+    "prefill": {"files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                "sha256": "78bf6fa31052f3336edf27ed8b602d89891a8732d2d859d6b7a1d44f04a935a4", "bytes_per_launch": 522343936},
+    # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
+    "decode": {"files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
+               "sha256": "cd2f0b5822aba3d400a9c178d01b3d3db17d173476f07ce74399531d28ca7f9c", "bytes_per_launch": 1201866048},
 }
 
 
-def source_sha(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def source_sha(rels):
+    h = hashlib.sha256()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def traffic_for(kernel):
     t = TRAFFIC[kernel]
     if t["sha256"] is None or t["bytes_per_launch"] is None:
         return None
-    return t["bytes_per_launch"] if source_sha(t["file"]) == t["sha256"] else None
+    return t["bytes_per_launch"] if source_sha(t["files"]) == t["sha256"] else None
 
 
 def load_peaks():
@@ -144,8 +149,8 @@ def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None):
         res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows)
         return time.perf_counter() - t0, flops, res.threads
 
-    dt, _, _ = run(64)
-    per_row = max(dt / 64, 1e-6)
+    dt, _, _ = run(2048)
+    per_row = max(dt / 2048, 1e-7)
     n = int(min(max_rows, max(64, target_s / per_row)))
     dt, flops, threads = run(n)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -399,7 +404,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile", action="store_true", help="no clock sampling (for ncu runs)")
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile:
