@@ -15,9 +15,10 @@
 // Work item: a 256-row query block of one (batch, head), split into two
 // 128-row query tiles X = A (rows 0..127) and X = B (rows 128..255) that
 // share every K and V tile.  A persistent grid of one CTA per SM walks the
-// items; 320 threads:
-//   warp 0       TMA producer: Q_A and Q_B of each item, then K_0, V_0,
-//                K_1, V_1, ... through one ring of shared-memory slots
+// items; 352 threads:
+//   warp 0       TMA producer of K_0, V_0, K_1, V_1, ... of every item
+//                through one ring of shared-memory slots
+//   warp 10      TMA producer of Q_A and Q_B of each item
 //   warp 1       tensor-memory allocation; one thread issues every MMA:
 //                S_X,j = Q_X K_j^T (both operands from shared memory, N = 128
 //                keys) and O_X += P_X,j V_j (P from tensor memory)
@@ -51,8 +52,9 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per tile
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr int kSoftmaxWarp0 = 2;                      // warps 2..5: tile A, 6..9: tile B
-constexpr int kThreads = 64 + 256;
+constexpr int kSoftmaxWarp0 = 2;  // warps 2..5: tile A, 6..9: tile B
+constexpr int kQWarp = 10;        // TMA producer of the Q tiles
+constexpr int kThreads = 64 + 256 + 32;
 
 template <int D>
 struct Cfg {
@@ -210,17 +212,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{wait_limit_ns, &g_err_prefill_bf16, abort_flag};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // Per item: Q_A, Q_B (each once its previous item's last S product is
-    // complete), then K_j and V_j for every key tile, through the ring.
-    if (lane == 0) {
+  if (warp == 0 || warp == kQWarp) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 10: Q_A and Q_B of each item, each once its previous item's last S
+    // product is complete.  Warp 0: K_j and V_j of every key tile of every
+    // item through the ring, independent of the Q loads, so the next item's
+    // first key tiles land while the current item is still running.
+    if (lane == 0 && warp == kQWarp) {
       prefetch_tensormap(&tmQ);
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-      const uint32_t full0 = bar(C::B_FULL), empty0 = bar(C::B_EMPTY);
       Sched sch(n_qp, BH, CAUSAL);
-      int bh, qp, n = 0;
+      int bh, qp;
       int nq[2] = {0, 0};  // Q_X copies issued
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
@@ -236,6 +237,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bar(C::B_QFULL + x), kb * 64, (2 * qp + x) * BM, bh);
           ++nq[x];
         }
+      }
+      if (*abort_flag) {
+        // let every copy still in flight land before the CTA can exit
+        for (int x = 0; x < 2; ++x)
+          if (nq[x] >= 1) mbar_wait_drain(bar(C::B_QFULL + x), (nq[x] - 1) & 1, kDrainLimitNs);
+      }
+    } else if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      const uint32_t full0 = bar(C::B_FULL), empty0 = bar(C::B_EMPTY);
+      Sched sch(n_qp, BH, CAUSAL);
+      int bh, qp, n = 0;
+      bool ok = true;
+      while (ok && sch.next(bh, qp)) {
+        const ItemShape sh(qp, S, CAUSAL);
         for (int j = 0; ok && j < 2 * sh.nkv; ++j, ++n) {
           const int st = n % C::NSLOT;
           if (n >= C::NSLOT &&
@@ -250,12 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         full0 + 8u * st, kb * 64, (j >> 1) * BN, bh);
         }
       }
-      if (*abort_flag) {
-        // let every copy still in flight land before the CTA can exit
-        drain_ring(full0, C::NSLOT, n);
-        for (int x = 0; x < 2; ++x)
-          if (nq[x] >= 1) mbar_wait_drain(bar(C::B_QFULL + x), (nq[x] - 1) & 1, kDrainLimitNs);
-      }
+      if (*abort_flag) drain_ring(full0, C::NSLOT, n);  // copies in flight land first
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -307,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j <= sh.nkv; ++j) {
           const int kidx = n + 2 * j, vidx = n + 2 * j - 1;  // K_j, V_j-1
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
+          // the operand tiles are normally resident long before they are
+          // needed; both waits come before the wait for P
           if (pv_step) ok = wait_slot(vidx, SITE_MMA_VFULL);
-          bool k_ready = false;
+          if (ok && s_step) ok = wait_slot(kidx, SITE_MMA_KFULL);
           for (int x = 0; ok && x < 2; ++x) {
             if (pv_step && j - 1 < nx[x]) {
               ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
@@ -322,12 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
             if (s_step && j < nx[x]) {
-              if (!k_ready) {
-                ok = wait_slot(kidx, SITE_MMA_KFULL);
-                if (!ok) break;
-                k_ready = true;
-                tc_fence_after();
-              }
+              tc_fence_after();
               issue_s(x, kidx);
               umma_commit(bar(C::B_SFULL + x));
               if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
