@@ -76,6 +76,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ------------------------------------------------------------------ ranks (weak scaling)
+RANK_SEED_STRIDE = 1000
+
+
+def rank_seed(base_seed, rank):
+    """Seed of a rank's own batch: every rank runs the same shape on different data."""
+    return base_seed + RANK_SEED_STRIDE * rank
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum over ranks of per-rank timings; every rank gets the result."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units processed by all ranks over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def prefill_flops(B, H, S, D, causal=True):
     return (2.0 if causal else 4.0) * B * H * S * S * D
 
@@ -223,16 +246,16 @@ def run_ours(args, rank, world, dist):
     do_decode = args.only in ("both", "decode")
     wp = si.WORKLOADS[PREFILL_WORKLOAD]
     wd = si.WORKLOADS[DECODE_WORKLOAD]
-    seed_shift = 1000 * rank  # each rank works on its own batch (weak scaling, no collective)
+    # each rank works on its own batch (weak scaling, no collective on the data path)
     if do_prefill:
-        xp = si.prefill_inputs(wp["B"], wp["H"], wp["S"], wp["D"], wp["seed"] + seed_shift,
+        xp = si.prefill_inputs(wp["B"], wp["H"], wp["S"], wp["D"], rank_seed(wp["seed"], rank),
                                qk_std=wp["qk_std"])
         Q, K, V = bf16_dev(xp.Q), bf16_dev(xp.K), bf16_dev(xp.V)
         O = torch.empty_like(Q)
         LSE = torch.empty((xp.B, xp.H, xp.S), dtype=torch.float32, device=dev)
         flops = prefill_flops(xp.B, xp.H, xp.S, xp.D, True)
     if do_decode:
-        xd = si.decode_inputs(wd["B"], wd["H"], wd["D"], wd["seed"] + seed_shift, wd["len_lo"],
+        xd = si.decode_inputs(wd["B"], wd["H"], wd["D"], rank_seed(wd["seed"], rank), wd["len_lo"],
                               wd["len_hi"])
         q, Kc, Vc = bf16_dev(xd.q), bf16_dev(xd.Kc), bf16_dev(xd.Vc)
         sl = torch.from_numpy(xd.seqlens).to(dev)
@@ -290,10 +313,7 @@ def run_ours(args, rank, world, dist):
     tp = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3  # s, prefill launches
     td = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3  # s, decode launches
     total = t_start.elapsed_time(t_end) / 1e3
-    times = torch.tensor([tp, td, total], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    tp, td, total = (float(v) for v in times.tolist())
+    tp, td, total = max_over_ranks([tp, td, total], dist, dev)
     launches = K_ * ((1 if do_prefill else 0) + ((1 + (nsplit > 1)) if do_decode else 0))
 
     # ---------------- end to end: pinned host buffers, copies inside the timed region
@@ -339,14 +359,11 @@ def run_ours(args, rank, world, dist):
         barrier()
         ep = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
         ed = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
-        et = torch.tensor([ep, ed], dtype=torch.float64, device=dev)
-        if dist is not None:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        ep, ed = (float(v) for v in et.tolist())
-        e2e = {"value": (world * E * flops / ep / 1e12) if do_prefill else None,
+        ep, ed = max_over_ranks([ep, ed], dist, dev)
+        e2e = {"value": (whole_job_rate(world, E * flops, ep) / 1e12) if do_prefill else None,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": E,
-               "decode_gbs": (world * E * dbytes / ed / 1e9) if do_decode else None,
+               "decode_gbs": (whole_job_rate(world, E * dbytes, ed) / 1e9) if do_decode else None,
                "path": "pinned host -> cudaMemcpyAsync -> C-ABI call -> cudaMemcpyAsync -> "
                        "pinned host, all on one stream"}
 
@@ -357,7 +374,7 @@ def run_ours(args, rank, world, dist):
     cfg = {"workload": PREFILL_WORKLOAD if do_prefill else DECODE_WORKLOAD,
            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
     if do_prefill:
-        value = world * K_ * flops / tp / 1e12
+        value = whole_job_rate(world, K_ * flops, tp) / 1e12
         per_launch_s = tp / K_
         achieved = flops / per_launch_s / 1e12
         line.update({"value": value, "unit": "TFLOP/s"})
@@ -371,7 +388,7 @@ def run_ours(args, rank, world, dist):
                     "kernel": "prefill_bf16_kernel<128, causal>", "us_per_launch": 1e6 * per_launch_s}
         line["roofline"] = roofline
     if do_decode:
-        gbs = world * K_ * dbytes / td / 1e9
+        gbs = whole_job_rate(world, K_ * dbytes, td) / 1e9
         cfg.update({"decode": {"B": xd.B, "H": xd.H, "D": xd.D, "len_range": [512, 8192],
                                "total_tokens": int(xd.seqlens.sum()), "splits": nsplit,
                                "bytes_per_step": dbytes}})
