@@ -15,18 +15,19 @@
 // Work item: a 256-row query block of one (batch, head), split into two
 // 128-row query tiles X = A (rows 0..127) and X = B (rows 128..255) that
 // share every K and V tile.  A persistent grid of one CTA per SM walks the
-// items; 352 threads:
+// items; 384 threads in three warpgroups (warp 3 idle), registers moved
+// from the control warpgroup to the softmax warpgroups with setmaxnreg:
 //   warp 0       TMA producer of K_0, V_0, K_1, V_1, ... of every item
 //                through one ring of shared-memory slots
-//   warp 10      TMA producer of Q_A and Q_B of each item
+//   warp 2       TMA producer of Q_A and Q_B of each item
 //   warp 1       tensor-memory allocation; one thread issues every MMA:
 //                S_X,j = Q_X K_j^T (both operands from shared memory, N = 128
 //                keys) and O_X += P_X,j V_j (P from tensor memory)
-//   warps 2..5   softmax of tile A, one query row per thread (128 keys per
+//   warps 4..7   softmax of tile A, one query row per thread (128 keys per
 //                row and tile), P_A,j written as bf16 over the columns of
 //                S_A,j; rescales O_A when the row's reference maximum moves;
 //                item epilogue O_A / l, log-sum-exp
-//   warps 6..9   the same for tile B
+//   warps 8..11  the same for tile B
 // The issuer orders each key step as P_A,j-1 V_j-1, S_A,j, P_B,j-1 V_j-1,
 // S_B,j: while one tile's softmax runs, the tensor pipe executes the other
 // tile's two products, so the chain softmax -> P V -> next S of one tile is
@@ -52,9 +53,18 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per tile
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr int kSoftmaxWarp0 = 2;  // warps 2..5: tile A, 6..9: tile B
-constexpr int kQWarp = 10;        // TMA producer of the Q tiles
-constexpr int kThreads = 64 + 256 + 32;
+// Largest fp32 weight sum of one tile kept without moving the reference
+// maximum (2^64): every weight is then <= 2^64, far inside fp32 and bf16 range.
+constexpr float kMaxTileWeight = 18446744073709551616.0f;
+constexpr int kSoftmaxWarp0 = 4;  // warps 4..7: tile A, 8..11: tile B
+constexpr int kQWarp = 2;         // TMA producer of the Q tiles
+constexpr int kThreads = 384;     // three warpgroups: control, softmax A, softmax B
+// Register split between the warpgroups (setmaxnreg).  The control
+// warpgroup returns registers that the softmax warpgroups take; the sum must
+// not exceed what the CTA was launched with (kThreads x kRegsLaunch), which
+// the host checks against the compiled kernel before every launch.
+constexpr int kRegsLaunch = 168, kRegsControl = 56, kRegsSoftmax = 224;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 
 template <int D>
 struct Cfg {
@@ -74,12 +84,18 @@ struct Cfg {
   static constexpr int B_PFULL = B_SFULL + 2;     // [X] P_X,j in TMEM, O_X rescaled (128 arrivals)
   static constexpr int B_OFULL = B_PFULL + 2;     // [X] the item's last P_X V complete
   static constexpr int B_OFREE = B_OFULL + 2;     // [X] O_X read by the epilogue (128 arrivals)
-  static constexpr int B_DRAIN = B_OFREE + 2;     // every MMA complete
+  static constexpr int B_SFREE = B_OFREE + 2;     // [X] S_X read by the softmax (split P; 128 arrivals)
+  static constexpr int B_PVDONE = B_SFREE + 2;    // [X] a P_X V complete (split P)
+  static constexpr int B_DRAIN = B_PVDONE + 2;    // every MMA complete
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + flags, alignment slack
   // tensor-memory columns: S_A, S_B (128 fp32 columns each; P_X is written
   // as bf16 pairs over the first 64 columns of S_X), then O_A, O_B
-  static constexpr uint32_t TM_S = 0, TM_O = 256;
+  // At D = 64 the accumulators leave room for P in columns of its own (split
+  // P): S_X,j+1 can then be computed while the softmax of tile j still runs.
+  // At D = 128 P is written over the first 64 columns of S_X.
+  static constexpr bool SPLIT_P = false;
+  static constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = SPLIT_P ? 384 : 256;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(NBAR * 8 + 8 <= 512, "barrier area");
   static_assert(TM_O + 2 * D <= TM_COLS, "tensor memory");
@@ -89,7 +105,7 @@ struct Cfg {
 // sites recorded with a timeout (bits 8.. of the error word)
 enum : uint32_t {
   SITE_PROD_EMPTY = 1, SITE_PROD_QEMPTY, SITE_MMA_Q, SITE_MMA_KFULL, SITE_MMA_VFULL,
-  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL
+  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL, SITE_MMA_SFREE, SITE_SM_PVDONE
 };
 
 // Key-tile counts of one item (query block qp of 256 rows).
@@ -198,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_FULL + s), 1);
       mbar_init(bar(C::B_EMPTY + s), 1);
     }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::B_SFREE + x), 128);
+      mbar_init(bar(C::B_PVDONE + x), 1);
+    }
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -211,10 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{wait_limit_ns, &g_err_prefill_bf16, abort_flag};
-
+  if (warp < 4) {
+  // control warpgroup: one register limit for all four warps, set at one place
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   if (warp == 0 || warp == kQWarp) {
     // ------------------------------------------------------------ TMA producers
-    // Warp 10: Q_A and Q_B of each item, each once its previous item's last S
+    // Warp 2: Q_A and Q_B of each item, each once its previous item's last S
     // product is complete.  Warp 0: K_j and V_j of every key tile of every
     // item through the ring, independent of the Q loads, so the next item's
     // first key tiles land while the current item is still running.
@@ -283,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Sched sch(n_qp, BH, CAUSAL);
       int bh, qp, n = 0;  // n: ring index of the item's K_0
       int nq[2] = {0, 0}, np[2] = {0, 0}, no[2] = {0, 0};  // Q_X items, P_X tiles, O_X items
+      int nsi[2] = {0, 0};  // S_X tiles issued (split P)
       bool ok = true;
       auto slot_of = [&](int idx) { return idx % C::NSLOT; };
       auto wait_slot = [&](int idx, uint32_t site) {
@@ -306,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int x, int idx, uint32_t acc) {
         const uint64_t vdesc = smem_desc_sw128(slot_addr(idx), C::BLOCK_BYTES, 1024);
         const uint32_t tO = tmem + C::TM_O + x * D;
-        const uint32_t tP = tmem + C::TM_S + x * 128;
+        const uint32_t tP = tmem + (C::SPLIT_P ? C::TM_P + x * 64 : C::TM_S + x * 128);
         umma_ts_mnmajor_x4(tO, tP, vdesc, idesc_o, acc);
         umma_ts_mnmajor_x4(tO, tP + 32, vdesc + (8192 >> 4), idesc_o, 1u);
       };
@@ -315,33 +338,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nx[2] = {sh.nA, sh.nB};
         for (int x = 0; ok && x < 2; ++x)
           if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), nq[x] & 1, wc, SITE_MMA_Q);
-        for (int j = 0; ok && j <= sh.nkv; ++j) {
-          const int kidx = n + 2 * j, vidx = n + 2 * j - 1;  // K_j, V_j-1
-          const bool s_step = j < sh.nkv, pv_step = j >= 1;
-          // the operand tiles are normally resident long before they are
-          // needed; both waits come before the wait for P
-          if (pv_step) ok = wait_slot(vidx, SITE_MMA_VFULL);
-          if (ok && s_step) ok = wait_slot(kidx, SITE_MMA_KFULL);
-          for (int x = 0; ok && x < 2; ++x) {
-            if (pv_step && j - 1 < nx[x]) {
+        if constexpr (C::SPLIT_P) {
+          // S_X,j+1 goes out as soon as the softmax has read S_X,j (S_FREE);
+          // P_X,j V_j as soon as P_X,j is written (P_FULL).  The two are in
+          // different tensor-memory columns, so neither waits for the other.
+          for (int j = -1; ok && j < sh.nkv; ++j) {
+            const int knext = n + 2 * (j + 1), vidx = n + 2 * j + 1;  // K_j+1, V_j
+            if (j + 1 < sh.nkv) {
+              ok = wait_slot(knext, SITE_MMA_KFULL);
+              for (int x = 0; ok && x < 2; ++x) {
+                if (j + 1 >= nx[x]) continue;
+                if (nsi[x] >= 1)
+                  ok = mbar_wait(bar(C::B_SFREE + x), (nsi[x] - 1) & 1, wc, SITE_MMA_SFREE);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(x, knext);
+                umma_commit(bar(C::B_SFULL + x));
+                ++nsi[x];
+                if (j + 1 == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
+              }
+              if (ok) umma_commit(bar(C::B_EMPTY + slot_of(knext)));
+            }
+            if (j < 0) continue;
+            if (ok) ok = wait_slot(vidx, SITE_MMA_VFULL);
+            for (int x = 0; ok && x < 2; ++x) {
+              if (j >= nx[x]) continue;
               ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
-              if (ok && j == 1 && no[x] >= 1)
+              if (ok && j == 0 && no[x] >= 1)
                 ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(x, vidx, j > 1 ? 1u : 0u);
+              issue_pv(x, vidx, j > 0 ? 1u : 0u);
+              umma_commit(bar(C::B_PVDONE + x));
               ++np[x];
-              if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
+              if (j == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
-            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
-            if (s_step && j < nx[x]) {
-              tc_fence_after();
-              issue_s(x, kidx);
-              umma_commit(bar(C::B_SFULL + x));
-              if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
-            }
+            if (ok) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
           }
-          if (ok && s_step) umma_commit(bar(C::B_EMPTY + slot_of(kidx)));
+        } else {
+          for (int j = 0; ok && j <= sh.nkv; ++j) {
+            const int kidx = n + 2 * j, vidx = n + 2 * j - 1;  // K_j, V_j-1
+            const bool s_step = j < sh.nkv, pv_step = j >= 1;
+            // the operand tiles are normally resident long before they are
+            // needed; both waits come before the wait for P
+            if (pv_step) ok = wait_slot(vidx, SITE_MMA_VFULL);
+            if (ok && s_step) ok = wait_slot(kidx, SITE_MMA_KFULL);
+            for (int x = 0; ok && x < 2; ++x) {
+              if (pv_step && j - 1 < nx[x]) {
+                ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
+                if (ok && j == 1 && no[x] >= 1)
+                  ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(x, vidx, j > 1 ? 1u : 0u);
+                ++np[x];
+                if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
+              }
+              if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
+              if (s_step && j < nx[x]) {
+                tc_fence_after();
+                issue_s(x, kidx);
+                umma_commit(bar(C::B_SFULL + x));
+                if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
+              }
+            }
+            if (ok && s_step) umma_commit(bar(C::B_EMPTY + slot_of(kidx)));
+          }
         }
         n += 2 * sh.nkv;
         for (int x = 0; x < 2; ++x)
@@ -355,7 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_DRAIN), 0, kDrainLimitNs);
     }
     __syncwarp();
+  }  // warp 3: no role
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax / epilogue
     // Warpgroup X owns query tile X; thread = one query row (TMEM lane).
     const int x = (warp - kSoftmaxWarp0) >> 2;
@@ -363,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
+    const uint32_t tP = tmem + lane_base + C::TM_P + x * 64;  // split P only
     const uint32_t tO = tmem + lane_base + C::TM_O + x * D;
     const uint32_t sfull = bar(C::B_SFULL + x), pfull = bar(C::B_PFULL + x);
     Sched sch(n_qp, BH, CAUSAL);
@@ -383,67 +448,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t s[128];
         tmem_ld_32x32b_x128(tS, s);
         const bool need_mask = CAUSAL ? (j == nx - 1) : (j * BN + BN > S);
-        if (need_mask) {
-          // last key index (within this tile) the row may use
-          const int lim = (CAUSAL ? min(q, S - 1) : (S - 1)) - j * BN;
+        // last key index (within this tile) the row may use
+        const int lim = (CAUSAL ? min(q, S - 1) : (S - 1)) - j * BN;
+        auto mask = [&](uint32_t (&v)[128]) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
-            if (i > lim) s[i] = __float_as_uint(-INFINITY);
-        }
-        // row maximum: eight independent chains, three-input max
-        float m8[8];
+            if (i > lim) v[i] = __float_as_uint(-INFINITY);
+        };
+        // row maximum in log2 units: eight independent chains, three-input max.
+        // Every row keeps at least its own key (causal) or key 0: it is finite.
+        auto row_max = [&](const uint32_t (&v)[128]) {
+          float m8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
+          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[k]), __uint_as_float(v[k + 8]));
 #pragma unroll
-        for (int i = 16; i < 128; i += 16)
+          for (int i = 16; i < 128; i += 16)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            m8[k] = max3f(m8[k], __uint_as_float(s[i + k]), __uint_as_float(s[i + 8 + k]));
-        const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
-                               fmaxf(m8[6], m8[7]));
-        // Every row keeps at least its own key (causal) or key 0, so mx is finite.
-        const float m_new = fmaxf(m_run, mx * c_log2);
-        // The reference maximum only moves when the row maximum has grown by
-        // more than 8 (log2 units): weights stay <= 256, exact in fp32 and in
-        // bf16's exponent range, and O is rescaled far less often.  Softmax is
-        // unchanged by the choice of reference, so this is exact arithmetic.
+            for (int k = 0; k < 8; ++k)
+              m8[k] = max3f(m8[k], __uint_as_float(v[i + k]), __uint_as_float(v[i + 8 + k]));
+          return c_log2 * max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                                fmaxf(m8[6], m8[7]));
+        };
+        if (need_mask) mask(s);
+        // Reference maximum m_use: the row maximum on an item's first tile;
+        // afterwards the running reference is kept as long as no weight of the
+        // tile exceeds 2^64 (checked through the tile's weight sum).  Weights up
+        // to 2^64 are exact in fp32 and bf16 range and their sums cannot
+        // overflow, so the row maximum of later tiles is never needed in the
+        // common case.  Softmax does not depend on the reference, so this is
+        // exact arithmetic.  A tile that does overflow (its scores exceed the
+        // reference by ~64, log2 units) is redone from tensor memory with its
+        // true maximum, and O is rescaled.
         const bool first = (j == 0);
-        const float m_use = (first || m_new > m_run + 8.0f) ? m_new : m_run;
+        float m_use = first ? row_max(s) : m_run;
         const float2 c2 = make_float2(c_log2, c_log2);
-        const float2 nm2 = make_float2(-m_use, -m_use);
-        // partial sums: the fp32 weights (for the log-sum-exp) and the
-        // bf16-rounded weights the P.V product uses (to normalise O, so that O
-        // is an exact convex combination of V rows)
-        float2 se[4];
-        float sr[8];
+        // P_X,j and its partial sums: the fp32 weights (for the log-sum-exp and
+        // the overflow check) and the bf16-rounded weights the P.V product uses
+        // (to normalise O, so that O is an exact convex combination of V rows)
+        uint32_t pk[2][32];
+        float rs, rsp;
+#pragma unroll 1
+        for (int pass = 0;; ++pass) {
+          const float2 nm2 = make_float2(-m_use, -m_use);
+          float2 se[4];
+          float sr[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
+          for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) sr[k] = 0.f;
+          for (int k = 0; k < 8; ++k) sr[k] = 0.f;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t p[32];
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e0 = 64 * h + 2 * i;
-            const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
-                                  c2, nm2);
-            const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
-            p[i] = pack_bf16x2(e.x, e.y);
-            se[i & 3] = add2(se[i & 3], e);
-            sr[(i & 3) * 2] = add_bf16_lo(p[i], sr[(i & 3) * 2]);
-            sr[(i & 3) * 2 + 1] = add_bf16_hi(p[i], sr[(i & 3) * 2 + 1]);
+            for (int i = 0; i < 32; ++i) {
+              const int e0 = 64 * h + 2 * i;
+              const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
+                                    c2, nm2);
+              const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
+              pk[h][i] = pack_bf16x2(e.x, e.y);
+              se[i & 3] = add2(se[i & 3], e);
+              sr[(i & 3) * 2] = add_bf16_lo(pk[h][i], sr[(i & 3) * 2]);
+              sr[(i & 3) * 2 + 1] = add_bf16_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+            }
           }
-          // keys 64h..64h+63 of P_X,j over S columns 32h..32h+31, already read
-          tmem_st_32x32b_x32(tS + 32 * h, p);
+          se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
+          rs = se[0].x + se[0].y;
+          rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+          const bool redo = pass == 0 && !first && !(rs <= kMaxTileWeight);  // also NaN / inf
+          if (!__any_sync(0xffffffffu, redo)) break;
+          // rare: the scores are still in tensor memory (P is stored below)
+          tmem_ld_32x32b_x128(tS, s);
+          if (need_mask) mask(s);
+          if (redo) m_use = fmaxf(m_run, row_max(s));
         }
-        se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
-        const float rs = se[0].x + se[0].y;
-        const float rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+        if constexpr (C::SPLIT_P) {
+          // the row is done with S: S_X,j+1 may overwrite these columns
+          tc_fence_before();
+          mbar_arrive(bar(C::B_SFREE + x));
+          // P_X,j-1 V_j-1 must have read the P columns (and finished O_X)
+          // before they are overwritten; it was issued when this warpgroup
+          // signalled P_X,j-1, a whole tile of softmax work ago.
+          if (ns >= 1) {
+            failed = !__all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + x), (ns - 1) & 1, wc,
+                                                        SITE_SM_PVDONE));
+            if (failed) break;
+            tc_fence_after();
+          }
+          tmem_st_32x32b_x32(tP, pk[0]);
+          tmem_st_32x32b_x32(tP + 32, pk[1]);
+        } else {
+          // P_X,j over the first 64 columns of S_X,j, which this thread has read
+          tmem_st_32x32b_x32(tS, pk[0]);
+          tmem_st_32x32b_x32(tS + 32, pk[1]);
+        }
         const bool resc = !first && (m_use != m_run);
         if (__any_sync(0xffffffffu, resc)) {
-          // S_X,j complete implies P_X,j-1 V_j-1 complete (issued before it by
-          // the same thread), so O_X is final through tile j - 1 here.
+          // O_X is final through tile j - 1 here: with P over S, S_X,j
+          // complete implies P_X,j-1 V_j-1 complete (issued before it by the
+          // same thread); with split P the P_V_DONE wait above saw it.
           const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -544,6 +645,13 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   auto kern = prefill_bf16_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // The softmax warpgroups raise their register limit with registers the
+  // control warpgroup returns; that only completes if the CTA was launched
+  // with at least kRegsLaunch registers per thread.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
   // persistent grid: one CTA per SM, each walking its share of the 256-row query blocks
   const long long items = static_cast<long long>(BH) * ((S + 2 * BM - 1) / (2 * BM));
   const int nsm = device_sm_count();

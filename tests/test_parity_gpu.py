@@ -71,6 +71,35 @@ def test_bf16_prefill_full(B, H, S, D, causal, qk_std):
                       what=f"B{B} H{H} S{S} D{D} causal={causal} std={qk_std}")
 
 
+def _scale_keys(t, lo, hi, factor):
+    """K with keys lo..hi-1 multiplied by a power of two (exact in bf16)."""
+    v = t.values.copy()
+    v[:, :, lo:hi, :] *= factor
+    bits = si.bf16_bits(v)
+    return si.Tensor(si.bf16_to_f32(bits), bits)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("which", ["later_keys_dominate", "first_keys_dominate"])
+def test_bf16_prefill_reference_moves(causal, D, which):
+    """Scores of some keys far above the others (x64): with later keys larger,
+    a row's reference maximum has to move by far more than 64 (log2 units)
+    after its first tile, which takes the kernel's re-do path (true maximum
+    from tensor memory, O rescaled); with the first keys larger, later tiles
+    underflow against the reference."""
+    S = 300
+    x = si.prefill_inputs(1, 2, S, D, seed=777 + D)
+    lo, hi = (128, S) if which == "later_keys_dominate" else (0, 128)
+    K = _scale_keys(x.K, lo, hi, 64.0)
+    O, L = mha().mha_fwd(dev_tensor(x.Q, torch.bfloat16), dev_tensor(K, torch.bfloat16),
+                         dev_tensor(x.V, torch.bfloat16), scale=x.scale, causal=causal)
+    Or, Lr = oracle.attention(x.Q.values, K.values, x.V.values, x.scale, causal)
+    assert float(np.max(Lr)) > 60.0  # the logits really are large
+    assert_bf16_close(O.float().cpu().numpy(), Or, L.cpu().numpy(), Lr,
+                      what=f"{which} D{D} causal={causal}")
+
+
 def test_bf16_prefill_without_lse_and_canary():
     x = si.prefill_inputs(1, 2, 200, 128, seed=4242)
     Q, K, V = (dev_tensor(t, torch.bfloat16) for t in (x.Q, x.K, x.V))
