@@ -84,18 +84,12 @@ struct Cfg {
   static constexpr int B_PFULL = B_SFULL + 2;     // [X] P_X,j in TMEM, O_X rescaled (128 arrivals)
   static constexpr int B_OFULL = B_PFULL + 2;     // [X] the item's last P_X V complete
   static constexpr int B_OFREE = B_OFULL + 2;     // [X] O_X read by the epilogue (128 arrivals)
-  static constexpr int B_SFREE = B_OFREE + 2;     // [X] S_X read by the softmax (split P; 128 arrivals)
-  static constexpr int B_PVDONE = B_SFREE + 2;    // [X] a P_X V complete (split P)
-  static constexpr int B_DRAIN = B_PVDONE + 2;    // every MMA complete
+  static constexpr int B_DRAIN = B_OFREE + 2;     // every MMA complete
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + flags, alignment slack
   // tensor-memory columns: S_A, S_B (128 fp32 columns each; P_X is written
   // as bf16 pairs over the first 64 columns of S_X), then O_A, O_B
-  // At D = 64 the accumulators leave room for P in columns of its own (split
-  // P): S_X,j+1 can then be computed while the softmax of tile j still runs.
-  // At D = 128 P is written over the first 64 columns of S_X.
-  static constexpr bool SPLIT_P = false;
-  static constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = SPLIT_P ? 384 : 256;
+  static constexpr uint32_t TM_S = 0, TM_O = 256;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(NBAR * 8 + 8 <= 512, "barrier area");
   static_assert(TM_O + 2 * D <= TM_COLS, "tensor memory");
@@ -105,7 +99,7 @@ struct Cfg {
 // sites recorded with a timeout (bits 8.. of the error word)
 enum : uint32_t {
   SITE_PROD_EMPTY = 1, SITE_PROD_QEMPTY, SITE_MMA_Q, SITE_MMA_KFULL, SITE_MMA_VFULL,
-  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL, SITE_MMA_SFREE, SITE_SM_PVDONE
+  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL
 };
 
 // Key-tile counts of one item (query block qp of 256 rows).
@@ -214,10 +208,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_FULL + s), 1);
       mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::B_SFREE + x), 128);
-      mbar_init(bar(C::B_PVDONE + x), 1);
-    }
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -305,7 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       Sched sch(n_qp, BH, CAUSAL);
       int bh, qp, n = 0;  // n: ring index of the item's K_0
       int nq[2] = {0, 0}, np[2] = {0, 0}, no[2] = {0, 0};  // Q_X items, P_X tiles, O_X items
-      int nsi[2] = {0, 0};  // S_X tiles issued (split P)
       bool ok = true;
       auto slot_of = [&](int idx) { return idx % C::NSLOT; };
       auto wait_slot = [&](int idx, uint32_t site) {
@@ -329,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int x, int idx, uint32_t acc) {
         const uint64_t vdesc = smem_desc_sw128(slot_addr(idx), C::BLOCK_BYTES, 1024);
         const uint32_t tO = tmem + C::TM_O + x * D;
-        const uint32_t tP = tmem + (C::SPLIT_P ? C::TM_P + x * 64 : C::TM_S + x * 128);
+        const uint32_t tP = tmem + C::TM_S + x * 128;
         umma_ts_mnmajor_x4(tO, tP, vdesc, idesc_o, acc);
         umma_ts_mnmajor_x4(tO, tP + 32, vdesc + (8192 >> 4), idesc_o, 1u);
       };
@@ -338,72 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nx[2] = {sh.nA, sh.nB};
         for (int x = 0; ok && x < 2; ++x)
           if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), nq[x] & 1, wc, SITE_MMA_Q);
-        if constexpr (C::SPLIT_P) {
-          // S_X,j+1 goes out as soon as the softmax has read S_X,j (S_FREE);
-          // P_X,j V_j as soon as P_X,j is written (P_FULL).  The two are in
-          // different tensor-memory columns, so neither waits for the other.
-          for (int j = -1; ok && j < sh.nkv; ++j) {
-            const int knext = n + 2 * (j + 1), vidx = n + 2 * j + 1;  // K_j+1, V_j
-            if (j + 1 < sh.nkv) {
-              ok = wait_slot(knext, SITE_MMA_KFULL);
-              for (int x = 0; ok && x < 2; ++x) {
-                if (j + 1 >= nx[x]) continue;
-                if (nsi[x] >= 1)
-                  ok = mbar_wait(bar(C::B_SFREE + x), (nsi[x] - 1) & 1, wc, SITE_MMA_SFREE);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(x, knext);
-                umma_commit(bar(C::B_SFULL + x));
-                ++nsi[x];
-                if (j + 1 == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
-              }
-              if (ok) umma_commit(bar(C::B_EMPTY + slot_of(knext)));
-            }
-            if (j < 0) continue;
-            if (ok) ok = wait_slot(vidx, SITE_MMA_VFULL);
-            for (int x = 0; ok && x < 2; ++x) {
-              if (j >= nx[x]) continue;
+        for (int j = 0; ok && j <= sh.nkv; ++j) {
+          const int kidx = n + 2 * j, vidx = n + 2 * j - 1;  // K_j, V_j-1
+          const bool s_step = j < sh.nkv, pv_step = j >= 1;
+          // the operand tiles are normally resident long before they are
+          // needed; both waits come before the wait for P
+          if (pv_step) ok = wait_slot(vidx, SITE_MMA_VFULL);
+          if (ok && s_step) ok = wait_slot(kidx, SITE_MMA_KFULL);
+          for (int x = 0; ok && x < 2; ++x) {
+            if (pv_step && j - 1 < nx[x]) {
               ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
-              if (ok && j == 0 && no[x] >= 1)
+              if (ok && j == 1 && no[x] >= 1)
                 ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(x, vidx, j > 0 ? 1u : 0u);
-              umma_commit(bar(C::B_PVDONE + x));
+              issue_pv(x, vidx, j > 1 ? 1u : 0u);
               ++np[x];
-              if (j == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
+              if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
-            if (ok) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
-          }
-        } else {
-          for (int j = 0; ok && j <= sh.nkv; ++j) {
-            const int kidx = n + 2 * j, vidx = n + 2 * j - 1;  // K_j, V_j-1
-            const bool s_step = j < sh.nkv, pv_step = j >= 1;
-            // the operand tiles are normally resident long before they are
-            // needed; both waits come before the wait for P
-            if (pv_step) ok = wait_slot(vidx, SITE_MMA_VFULL);
-            if (ok && s_step) ok = wait_slot(kidx, SITE_MMA_KFULL);
-            for (int x = 0; ok && x < 2; ++x) {
-              if (pv_step && j - 1 < nx[x]) {
-                ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
-                if (ok && j == 1 && no[x] >= 1)
-                  ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(x, vidx, j > 1 ? 1u : 0u);
-                ++np[x];
-                if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
-              }
-              if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
-              if (s_step && j < nx[x]) {
-                tc_fence_after();
-                issue_s(x, kidx);
-                umma_commit(bar(C::B_SFULL + x));
-                if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
-              }
+            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
+            if (s_step && j < nx[x]) {
+              tc_fence_after();
+              issue_s(x, kidx);
+              umma_commit(bar(C::B_SFULL + x));
+              if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
             }
-            if (ok && s_step) umma_commit(bar(C::B_EMPTY + slot_of(kidx)));
           }
+          if (ok && s_step) umma_commit(bar(C::B_EMPTY + slot_of(kidx)));
         }
         n += 2 * sh.nkv;
         for (int x = 0; x < 2; ++x)
@@ -427,7 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
-    const uint32_t tP = tmem + lane_base + C::TM_P + x * 64;  // split P only
     const uint32_t tO = tmem + lane_base + C::TM_O + x * D;
     const uint32_t sfull = bar(C::B_SFULL + x), pfull = bar(C::B_PFULL + x);
     Sched sch(n_qp, BH, CAUSAL);
@@ -520,31 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (need_mask) mask(s);
           if (redo) m_use = fmaxf(m_run, row_max(s));
         }
-        if constexpr (C::SPLIT_P) {
-          // the row is done with S: S_X,j+1 may overwrite these columns
-          tc_fence_before();
-          mbar_arrive(bar(C::B_SFREE + x));
-          // P_X,j-1 V_j-1 must have read the P columns (and finished O_X)
-          // before they are overwritten; it was issued when this warpgroup
-          // signalled P_X,j-1, a whole tile of softmax work ago.
-          if (ns >= 1) {
-            failed = !__all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + x), (ns - 1) & 1, wc,
-                                                        SITE_SM_PVDONE));
-            if (failed) break;
-            tc_fence_after();
-          }
-          tmem_st_32x32b_x32(tP, pk[0]);
-          tmem_st_32x32b_x32(tP + 32, pk[1]);
-        } else {
-          // P_X,j over the first 64 columns of S_X,j, which this thread has read
-          tmem_st_32x32b_x32(tS, pk[0]);
-          tmem_st_32x32b_x32(tS + 32, pk[1]);
-        }
+        // P_X,j over the first 64 columns of S_X,j, which this thread has read
+        tmem_st_32x32b_x32(tS, pk[0]);
+        tmem_st_32x32b_x32(tS + 32, pk[1]);
         const bool resc = !first && (m_use != m_run);
         if (__any_sync(0xffffffffu, resc)) {
-          // O_X is final through tile j - 1 here: with P over S, S_X,j
-          // complete implies P_X,j-1 V_j-1 complete (issued before it by the
-          // same thread); with split P the P_V_DONE wait above saw it.
+          // S_X,j complete implies P_X,j-1 V_j-1 complete (issued before it by
+          // the same thread), so O_X is final through tile j - 1 here.
           const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {

@@ -436,12 +436,12 @@ __device__ __forceinline__ float add_bf16_hi(uint32_t w, float acc) {
 // 2^x for a pair, on the FMA pipe: x = n + f with n = round(x) (the 1.5*2^23
 // shifter leaves n in the low mantissa bits), 2^f from the degree-3 minimax
 // polynomial of exp2_poly.h, then n is added to the exponent field.  x is
-// clamped to >= -126 so the exponent add cannot leave the normal range.
+// clamped to [-126, 127] so the exponent add cannot leave the normal range.
 // Relative error <= 7.5e-5 plus fp32 rounding.
 __device__ __forceinline__ float2 exp2_poly2(float2 x) {
   constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -126.0f);
-  x.y = fmaxf(x.y, -126.0f);
+  x.x = fminf(fmaxf(x.x, -126.0f), 127.0f);
+  x.y = fminf(fmaxf(x.y, -126.0f), 127.0f);
   const float2 t = add2(x, make_float2(kShift, kShift));
   const float2 n = add2(t, make_float2(-kShift, -kShift));
   const float2 f = fma2(n, make_float2(-1.0f, -1.0f), x);

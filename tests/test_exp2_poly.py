@@ -34,7 +34,7 @@ def fma32(a, b, c):
 def exp2_poly(x):
     c = coeffs()
     shift = np.float32(12582912.0)
-    x = np.maximum(f32(x), np.float32(-126.0))
+    x = np.minimum(np.maximum(f32(x), np.float32(-126.0)), np.float32(127.0))
     t = f32(x.astype(np.float64) + shift)
     n = f32(t.astype(np.float64) - shift)
     f = fma32(n, np.full_like(n, -1.0), x)
@@ -46,11 +46,12 @@ def exp2_poly(x):
 
 
 def test_relative_error_over_kernel_range():
-    # the kernel's exponent arguments lie in [-inf, 8]; below -126 it clamps, and
-    # within one unit of the clamp the result reaches the denormal boundary (~1e-38)
-    x = np.concatenate([np.linspace(-125.0, 8.0, 2_000_001, dtype=np.float64),
-                        np.arange(-125, 9, dtype=np.float64),
-                        np.arange(-125, 8, dtype=np.float64) + 0.5]).astype(np.float32)
+    # the kernel's exponent arguments lie in [-inf, 64] on its fast path; below
+    # -126 it clamps, and within one unit of the clamp the result reaches the
+    # denormal boundary (~1e-38)
+    x = np.concatenate([np.linspace(-125.0, 126.0, 2_000_001, dtype=np.float64),
+                        np.arange(-125, 127, dtype=np.float64),
+                        np.arange(-125, 126, dtype=np.float64) + 0.5]).astype(np.float32)
     y = exp2_poly(x).astype(np.float64)
     ref = np.exp2(x.astype(np.float64))
     rel = np.abs(y / ref - 1.0)
@@ -61,6 +62,13 @@ def test_relative_error_over_kernel_range():
 def test_clamped_inputs_stay_tiny_and_positive():
     y = exp2_poly(np.array([-np.inf, -1e30, -500.0, -127.0, -126.5, -125.5], np.float32))
     assert np.all(y > 0) and np.all(y < 2.0 ** -124)
+
+
+def test_large_inputs_stay_huge_and_finite():
+    # above 127 the input is clamped: the result stays >= 2^127, so a weight
+    # past the kernel's 2^64 bound is still seen as one (never wraps to small)
+    y = exp2_poly(np.array([127.0, 128.0, 200.0, 1e30, np.inf], np.float32))
+    assert np.all(np.isfinite(y)) and np.all(y >= 2.0 ** 126)
 
 
 def test_generator_reproduces_header():
