@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     # profiles/prefill_bf16_d128_causal_b4h32s4096.md
     "prefill": {"files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "4bff5907e501e0e031d27c1db0c250e0ba85adade8a3e33e97b91330c09cc3ec", "bytes_per_launch": 518117376},
+                "sha256": "f90c161360a2f55ac1daa27663d188c3661c2482b657e51ce79590ff7e482c20", "bytes_per_launch": 516880640},
     # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
     "decode": {"files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                "sha256": "cd2f0b5822aba3d400a9c178d01b3d3db17d173476f07ce74399531d28ca7f9c", "bytes_per_launch": 1201866048},
