@@ -157,7 +157,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None):
+def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None, workload=PREFILL_WORKLOAD):
     """Time the fp64 oracle on random rows of the prefill workload for about target_s."""
     import oracle
     rng = np.random.default_rng(seed)
@@ -177,7 +177,7 @@ def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None):
     n = int(min(max_rows, max(64, target_s / per_row)))
     dt, flops, threads = run(n)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} random query rows of {PREFILL_WORKLOAD} (causal), "
+            "sample": f"{n} random query rows of {workload} (causal), "
                       f"fp64 C oracle, {dt:.1f} s"}
 
 
@@ -186,8 +186,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import oracle
-    w = si.WORKLOADS[PREFILL_WORKLOAD]
-    x = si.workload_inputs(PREFILL_WORKLOAD)
+    w = si.WORKLOADS[args.prefill_workload]
+    x = si.workload_inputs(args.prefill_workload)
     rng = np.random.default_rng(123)
     total_rows = x.B * x.H * x.S
     budget_per_step = min(1.0, 150.0 / max(1, args.steps + args.warmup))
@@ -215,10 +215,10 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL_WORKLOAD, "B": w["B"], "H": w["H"], "S": w["S"],
+        "config": {"workload": args.prefill_workload, "B": w["B"], "H": w["H"], "S": w["S"],
                    "D": w["D"], "causal": True, "sample_rows_per_step": n},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{n} random query rows per step of {PREFILL_WORKLOAD}"},
+                         "sample": f"{n} random query rows per step of {args.prefill_workload}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -244,7 +244,7 @@ def run_ours(args, rank, world, dist):
 
     do_prefill = args.only in ("both", "prefill")
     do_decode = args.only in ("both", "decode")
-    wp = si.WORKLOADS[PREFILL_WORKLOAD]
+    wp = si.WORKLOADS[args.prefill_workload]
     wd = si.WORKLOADS[DECODE_WORKLOAD]
     # each rank works on its own batch (weak scaling, no collective on the data path)
     if do_prefill:
@@ -371,7 +371,7 @@ def run_ours(args, rank, world, dist):
         return 0
 
     line = {"impl": "ours", "metric": METRIC}
-    cfg = {"workload": PREFILL_WORKLOAD if do_prefill else DECODE_WORKLOAD,
+    cfg = {"workload": args.prefill_workload if do_prefill else DECODE_WORKLOAD,
            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
     if do_prefill:
         value = whole_job_rate(world, K_ * flops, tp) / 1e12
@@ -379,13 +379,14 @@ def run_ours(args, rank, world, dist):
         achieved = flops / per_launch_s / 1e12
         line.update({"value": value, "unit": "TFLOP/s"})
         cfg.update({"prefill": {"B": xp.B, "H": xp.H, "S": xp.S, "D": xp.D, "causal": True,
-                                "qk_std": 3.0, "flops_per_step": flops}})
+                                "qk_std": wp["qk_std"], "flops_per_step": flops}})
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "traffic": traffic_for("prefill"),
+                    # the recorded counters belong to the default workload only
+                    "traffic": traffic_for("prefill") if args.prefill_workload == PREFILL_WORKLOAD else None,
                     "peak_source": f"bf16_tflops (burst), of {peak_src}",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "kernel": "prefill_bf16_kernel<128, causal>", "us_per_launch": 1e6 * per_launch_s}
+                    "kernel": f"prefill_bf16_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
         line["roofline"] = roofline
     if do_decode:
         gbs = whole_job_rate(world, K_ * dbytes, td) / 1e9
@@ -406,7 +407,7 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": launches,
     })
     if not args.no_cpu_baseline and world == 1 and do_prefill:
-        line["cpu_baseline"] = oracle_sample_tflops(xp, args.cpu_seconds)
+        line["cpu_baseline"] = oracle_sample_tflops(xp, args.cpu_seconds, workload=args.prefill_workload)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -418,6 +419,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--only", choices=("both", "prefill", "decode"), default="both")
+    ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
+                    choices=[k for k, w in si.WORKLOADS.items()
+                             if w["kind"] == "prefill" and w["dtype"] == "bf16"],
+                    help="bf16 prefill workload of the step (default: the headline one)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
