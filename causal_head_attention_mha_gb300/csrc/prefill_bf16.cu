@@ -71,16 +71,22 @@ struct Cfg {
   static constexpr int KB = D / 64;               // 128-byte column blocks per row
   static constexpr int BLOCK_BYTES = 128 * 128;   // one 128-row x 64-col bf16 block
   static constexpr int TILE_BYTES = KB * BLOCK_BYTES;
-  static constexpr int NSLOT = (D == 128) ? 5 : 12;  // ring slots, each one K or one V tile
+  // Ring of K/V units.  D = 64: a unit holds K_j and V_j of one key tile
+  // (one wait and one release per key step; 6 units leave ample lead).
+  // D = 128: a unit holds one K or one V tile (5 units; pairing them would
+  // leave only 2 units and too little lead for the loads).
+  static constexpr bool PAIRED = (D == 64);
+  static constexpr int NUNIT = PAIRED ? 6 : 5;
+  static constexpr int UNIT_BYTES = (PAIRED ? 2 : 1) * TILE_BYTES;
   static constexpr int Q_OFF = 0;                 // Q_A, Q_B
   static constexpr int RING_OFF = 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + NSLOT * TILE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + NUNIT * UNIT_BYTES;
   // barrier indices ([X] = one per query tile)
   static constexpr int B_QFULL = 0;               // [X] Q_X landed
   static constexpr int B_QEMPTY = 2;              // [X] the item's last S_X complete
-  static constexpr int B_FULL = 4;                // [slot] a K or V tile landed
-  static constexpr int B_EMPTY = B_FULL + NSLOT;  // [slot] its last reader complete
-  static constexpr int B_SFULL = B_EMPTY + NSLOT; // [X] S_X,j in TMEM
+  static constexpr int B_FULL = 4;                 // [unit] its tiles landed
+  static constexpr int B_EMPTY = B_FULL + NUNIT;   // [unit] their last reader complete
+  static constexpr int B_SFULL = B_EMPTY + NUNIT;  // [X] S_X,j in TMEM
   static constexpr int B_PFULL = B_SFULL + 2;     // [X] P_X,j in TMEM, O_X rescaled (128 arrivals)
   static constexpr int B_OFULL = B_PFULL + 2;     // [X] the item's last P_X V complete
   static constexpr int B_OFREE = B_OFULL + 2;     // [X] O_X read by the epilogue (128 arrivals)
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_OFULL + x), 1);
       mbar_init(bar(C::B_OFREE + x), 128);
     }
-    for (int s = 0; s < C::NSLOT; ++s) {
+    for (int s = 0; s < C::NUNIT; ++s) {
       mbar_init(bar(C::B_FULL + s), 1);
       mbar_init(bar(C::B_EMPTY + s), 1);
     }
@@ -264,21 +270,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
         const ItemShape sh(qp, S, CAUSAL);
-        for (int j = 0; ok && j < 2 * sh.nkv; ++j, ++n) {
-          const int st = n % C::NSLOT;
-          if (n >= C::NSLOT &&
-              !mbar_wait(empty0 + 8u * st, ((n / C::NSLOT) & 1) ^ 1, wc, SITE_PROD_EMPTY)) {
+        // units in order: K_0 V_0 K_1 V_1 ... (paired: one unit per key tile)
+        const int nunits = (C::PAIRED ? 1 : 2) * sh.nkv;
+        for (int u = 0; ok && u < nunits; ++u, ++n) {
+          const int st = n % C::NUNIT;
+          if (n >= C::NUNIT &&
+              !mbar_wait(empty0 + 8u * st, ((n / C::NUNIT) & 1) ^ 1, wc, SITE_PROD_EMPTY)) {
             ok = false;
             break;
           }
-          const CUtensorMap* map = (j & 1) ? &tmV : &tmK;
-          mbar_arrive_expect_tx(full0 + 8u * st, C::TILE_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(sbase + C::RING_OFF + st * C::TILE_BYTES + kb * C::BLOCK_BYTES, map,
-                        full0 + 8u * st, kb * 64, (j >> 1) * BN, bh);
+          const uint32_t dst = sbase + C::RING_OFF + st * C::UNIT_BYTES;
+          const int j = C::PAIRED ? u : (u >> 1);  // key tile
+          mbar_arrive_expect_tx(full0 + 8u * st, C::UNIT_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            if (C::PAIRED || !(u & 1))
+              tma_load_3d(dst + kb * C::BLOCK_BYTES, &tmK, full0 + 8u * st, kb * 64, j * BN, bh);
+            if (C::PAIRED || (u & 1))
+              tma_load_3d(dst + (C::PAIRED ? C::TILE_BYTES : 0) + kb * C::BLOCK_BYTES, &tmV,
+                          full0 + 8u * st, kb * 64, j * BN, bh);
+          }
         }
       }
-      if (*abort_flag) drain_ring(full0, C::NSLOT, n);  // copies in flight land first
+      if (*abort_flag) drain_ring(full0, C::NUNIT, n);  // copies in flight land first
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -293,30 +306,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       Sched sch(n_qp, BH, CAUSAL);
-      int bh, qp, n = 0;  // n: ring index of the item's K_0
+      int bh, qp, n = 0;  // n: ring unit index of the item's first unit (K_0)
       int nq[2] = {0, 0}, np[2] = {0, 0}, no[2] = {0, 0};  // Q_X items, P_X tiles, O_X items
       bool ok = true;
-      auto slot_of = [&](int idx) { return idx % C::NSLOT; };
-      auto wait_slot = [&](int idx, uint32_t site) {
-        return mbar_wait(bar(C::B_FULL + slot_of(idx)), (idx / C::NSLOT) & 1, wc, site);
+      auto unit_of = [&](int u) { return u % C::NUNIT; };
+      auto unit_addr = [&](int u) {
+        return sbase + C::RING_OFF + static_cast<uint32_t>(unit_of(u)) * C::UNIT_BYTES;
       };
-      auto slot_addr = [&](int idx) {
-        return sbase + C::RING_OFF + static_cast<uint32_t>(slot_of(idx)) * C::TILE_BYTES;
+      auto wait_unit = [&](int u, uint32_t site) {
+        return mbar_wait(bar(C::B_FULL + unit_of(u)), (u / C::NUNIT) & 1, wc, site);
       };
-      // S_X = Q_X K^T, K tile at ring index idx (K-major operands, LBO unused)
-      auto issue_s = [&](int x, int idx) {
+      // ring units of K_j and V_j of the current item, and their addresses
+      auto k_unit = [&](int j) { return C::PAIRED ? n + j : n + 2 * j; };
+      auto v_unit = [&](int j) { return C::PAIRED ? n + j : n + 2 * j + 1; };
+      auto v_off = C::PAIRED ? C::TILE_BYTES : 0;
+      // S_X = Q_X K_j^T (K-major operands, LBO unused)
+      auto issue_s = [&](int x, int j) {
         const uint64_t qdesc = smem_desc_sw128(sbase + C::Q_OFF + x * C::TILE_BYTES, 16, 1024);
-        const uint64_t kdesc = smem_desc_sw128(slot_addr(idx), 16, 1024);
+        const uint64_t kdesc = smem_desc_sw128(unit_addr(k_unit(j)), 16, 1024);
         const uint32_t tS = tmem + C::TM_S + x * 128;
         if constexpr (D == 128)
           umma_ss_kmajor_x8(tS, qdesc, kdesc, idesc_s, 0u);
         else
           umma_ss_kmajor_x4(tS, qdesc, kdesc, idesc_s, 0u);
       };
-      // O_X (+)= P_X V, V tile at ring index idx: MN-major, LBO = next 64
-      // columns of D, keys 64.. start 64 rows (8 KB) into each block
-      auto issue_pv = [&](int x, int idx, uint32_t acc) {
-        const uint64_t vdesc = smem_desc_sw128(slot_addr(idx), C::BLOCK_BYTES, 1024);
+      // O_X (+)= P_X V_j: V MN-major, LBO = next 64 columns of D, keys 64..
+      // start 64 rows (8 KB) into each block
+      auto issue_pv = [&](int x, int j, uint32_t acc) {
+        const uint64_t vdesc = smem_desc_sw128(unit_addr(v_unit(j)) + v_off, C::BLOCK_BYTES, 1024);
         const uint32_t tO = tmem + C::TM_O + x * D;
         const uint32_t tP = tmem + C::TM_S + x * 128;
         umma_ts_mnmajor_x4(tO, tP, vdesc, idesc_o, acc);
@@ -328,12 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; ok && x < 2; ++x)
           if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), nq[x] & 1, wc, SITE_MMA_Q);
         for (int j = 0; ok && j <= sh.nkv; ++j) {
-          const int kidx = n + 2 * j, vidx = n + 2 * j - 1;  // K_j, V_j-1
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
-          // the operand tiles are normally resident long before they are
-          // needed; both waits come before the wait for P
-          if (pv_step) ok = wait_slot(vidx, SITE_MMA_VFULL);
-          if (ok && s_step) ok = wait_slot(kidx, SITE_MMA_KFULL);
+          // the operand waits (normally met long before) come before the wait
+          // for P; paired units bring V_j-1 with K_j-1, waited at step j - 1
+          if (!C::PAIRED && pv_step) ok = wait_unit(v_unit(j - 1), SITE_MMA_VFULL);
+          if (ok && s_step) ok = wait_unit(k_unit(j), SITE_MMA_KFULL);
           for (int x = 0; ok && x < 2; ++x) {
             if (pv_step && j - 1 < nx[x]) {
               ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
@@ -341,21 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(x, vidx, j > 1 ? 1u : 0u);
+              issue_pv(x, j - 1, j > 1 ? 1u : 0u);
               ++np[x];
               if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
-            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + slot_of(vidx)));
+            // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1,
+            // whose S products came before)
+            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + unit_of(v_unit(j - 1))));
             if (s_step && j < nx[x]) {
               tc_fence_after();
-              issue_s(x, kidx);
+              issue_s(x, j);
               umma_commit(bar(C::B_SFULL + x));
               if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
             }
           }
-          if (ok && s_step) umma_commit(bar(C::B_EMPTY + slot_of(kidx)));
+          // K_j's last reader is S_B,j (unpaired units only)
+          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + unit_of(k_unit(j))));
         }
-        n += 2 * sh.nkv;
+        n += (C::PAIRED ? 1 : 2) * sh.nkv;
         for (int x = 0; x < 2; ++x)
           if (nx[x] > 0) {
             ++nq[x];
