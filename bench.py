@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     # profiles/prefill_bf16_d128_causal_b4h32s4096.md
     "prefill": {"files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "f90c161360a2f55ac1daa27663d188c3661c2482b657e51ce79590ff7e482c20", "bytes_per_launch": 516880640},
+                "sha256": "d167eece1e8be2fb14b187ead9c4b133e14fd121dfde2e712255de406c471c50", "bytes_per_launch": 517964544},
     # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
     "decode": {"files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                "sha256": "cd2f0b5822aba3d400a9c178d01b3d3db17d173476f07ce74399531d28ca7f9c", "bytes_per_launch": 1201866048},

@@ -71,6 +71,21 @@ def test_bf16_prefill_full(B, H, S, D, causal, qk_std):
                       what=f"B{B} H{H} S{S} D{D} causal={causal} std={qk_std}")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_bf16_prefill_many_items_per_cta(causal, D):
+    """Every output compared on a workload with several 256-row work items
+    per CTA of the persistent grid (B*H*ceil(S/256) = 960 items), so the K/V
+    ring and every barrier phase carry over from item to item; S = 600 also
+    leaves the last query block of each head without its second tile."""
+    x = si.prefill_inputs(8, 40, 600, D, seed=5150 + D)
+    O, L = mha().mha_fwd(dev_tensor(x.Q, torch.bfloat16), dev_tensor(x.K, torch.bfloat16),
+                         dev_tensor(x.V, torch.bfloat16), scale=x.scale, causal=causal)
+    Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal)
+    assert_bf16_close(O.float().cpu().numpy(), Or, L.cpu().numpy(), Lr,
+                      what=f"B8 H40 S600 D{D} causal={causal}")
+
+
 def _scale_keys(t, lo, hi, factor):
     """K with keys lo..hi-1 multiplied by a power of two (exact in bf16)."""
     v = t.values.copy()
