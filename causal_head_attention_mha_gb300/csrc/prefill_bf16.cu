@@ -306,39 +306,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       Sched sch(n_qp, BH, CAUSAL);
-      int bh, qp, n = 0;  // n: ring unit index of the item's first unit (K_0)
+      int bh, qp;
       int nq[2] = {0, 0}, np[2] = {0, 0}, no[2] = {0, 0};  // Q_X items, P_X tiles, O_X items
       bool ok = true;
-      auto unit_of = [&](int u) { return u % C::NUNIT; };
-      auto unit_addr = [&](int u) {
-        return sbase + C::RING_OFF + static_cast<uint32_t>(unit_of(u)) * C::UNIT_BYTES;
+      // The ring units are consumed in index order (K_0 V_0 K_1 V_1 ..., or
+      // one unit per key tile when paired), so a cursor (slot, phase) walks
+      // them; the operand descriptors are fixed bases plus the slot offset
+      // (shared-memory addresses stay below 2^18, so the 14-bit address field
+      // of the descriptor cannot carry).
+      int cur_slot = 0;
+      uint32_t cur_phase = 0;
+      auto take = [&](int& slot, uint32_t& phase) {
+        slot = cur_slot;
+        phase = cur_phase;
+        if (++cur_slot == C::NUNIT) {
+          cur_slot = 0;
+          cur_phase ^= 1u;
+        }
       };
-      auto wait_unit = [&](int u, uint32_t site) {
-        return mbar_wait(bar(C::B_FULL + unit_of(u)), (u / C::NUNIT) & 1, wc, site);
-      };
-      // ring units of K_j and V_j of the current item, and their addresses
-      auto k_unit = [&](int j) { return C::PAIRED ? n + j : n + 2 * j; };
-      auto v_unit = [&](int j) { return C::PAIRED ? n + j : n + 2 * j + 1; };
-      auto v_off = C::PAIRED ? C::TILE_BYTES : 0;
-      // S_X = Q_X K_j^T (K-major operands, LBO unused)
-      auto issue_s = [&](int x, int j) {
-        const uint64_t qdesc = smem_desc_sw128(sbase + C::Q_OFF + x * C::TILE_BYTES, 16, 1024);
-        const uint64_t kdesc = smem_desc_sw128(unit_addr(k_unit(j)), 16, 1024);
-        const uint32_t tS = tmem + C::TM_S + x * 128;
-        if constexpr (D == 128)
-          umma_ss_kmajor_x8(tS, qdesc, kdesc, idesc_s, 0u);
-        else
-          umma_ss_kmajor_x4(tS, qdesc, kdesc, idesc_s, 0u);
-      };
-      // O_X (+)= P_X V_j: V MN-major, LBO = next 64 columns of D, keys 64..
-      // start 64 rows (8 KB) into each block
-      auto issue_pv = [&](int x, int j, uint32_t acc) {
-        const uint64_t vdesc = smem_desc_sw128(unit_addr(v_unit(j)) + v_off, C::BLOCK_BYTES, 1024);
-        const uint32_t tO = tmem + C::TM_O + x * D;
-        const uint32_t tP = tmem + C::TM_S + x * 128;
-        umma_ts_mnmajor_x4(tO, tP, vdesc, idesc_o, acc);
-        umma_ts_mnmajor_x4(tO, tP + 32, vdesc + (8192 >> 4), idesc_o, 1u);
-      };
+      // low 32 bits of a descriptor: start address >> 4 (bits 0-13) and
+      // LBO >> 4 (bits 16-29); the high word (SBO = 1024, fixed bits) is the
+      // same for every operand here
+      const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
+      auto desc = [&](uint32_t lo) { return (static_cast<uint64_t>(desc_hi) << 32) | lo; };
+      const uint32_t ring_lo = (sbase + C::RING_OFF) >> 4;
+      const uint32_t q_lo = ((sbase + C::Q_OFF) >> 4) | (1u << 16);
+      constexpr uint32_t kUnitLo = C::UNIT_BYTES >> 4;
+      constexpr uint32_t kVLo = ((C::PAIRED ? C::TILE_BYTES : 0) >> 4) | ((C::BLOCK_BYTES >> 4) << 16);
+      int k_slot = 0, v_slot = 0;  // ring slots of K_j and V_j-1 at this step
+      uint32_t k_phase = 0, v_phase = 0;
       while (ok && sch.next(bh, qp)) {
         const ItemShape sh(qp, S, CAUSAL);
         const int nx[2] = {sh.nA, sh.nB};
@@ -346,10 +342,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), nq[x] & 1, wc, SITE_MMA_Q);
         for (int j = 0; ok && j <= sh.nkv; ++j) {
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
+          // this step's units: V_j-1 (unpaired: its own unit; paired: the
+          // unit of K_j-1, taken at step j - 1), then K_j
+          if (pv_step) {
+            if constexpr (C::PAIRED) {
+              v_slot = k_slot;
+              v_phase = k_phase;
+            } else {
+              take(v_slot, v_phase);
+            }
+          }
+          if (s_step) take(k_slot, k_phase);
           // the operand waits (normally met long before) come before the wait
-          // for P; paired units bring V_j-1 with K_j-1, waited at step j - 1
-          if (!C::PAIRED && pv_step) ok = wait_unit(v_unit(j - 1), SITE_MMA_VFULL);
-          if (ok && s_step) ok = wait_unit(k_unit(j), SITE_MMA_KFULL);
+          // for P; a paired unit was waited for when its K was needed
+          if (!C::PAIRED && pv_step) ok = mbar_wait(bar(C::B_FULL + v_slot), v_phase, wc, SITE_MMA_VFULL);
+          if (ok && s_step) ok = mbar_wait(bar(C::B_FULL + k_slot), k_phase, wc, SITE_MMA_KFULL);
+          const uint32_t k_lo = ring_lo + static_cast<uint32_t>(k_slot) * kUnitLo + (1u << 16);
+          const uint32_t v_lo = ring_lo + static_cast<uint32_t>(v_slot) * kUnitLo + kVLo;
           for (int x = 0; ok && x < 2; ++x) {
             if (pv_step && j - 1 < nx[x]) {
               ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
@@ -357,24 +366,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(x, j - 1, j > 1 ? 1u : 0u);
+              // O_X (+)= P_X V_j-1: V MN-major, LBO = next 64 columns of D,
+              // keys 64.. start 64 rows (8 KB) into each block
+              const uint32_t tO = tmem + C::TM_O + x * D, tP = tmem + C::TM_S + x * 128;
+              const uint32_t acc = j > 1 ? 1u : 0u;
+              umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
+              umma_ts_mnmajor_x4(tO, tP + 32, desc(v_lo + (8192 >> 4)), idesc_o, 1u);
               ++np[x];
               if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
             // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1,
             // whose S products came before)
-            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + unit_of(v_unit(j - 1))));
+            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + v_slot));
             if (s_step && j < nx[x]) {
               tc_fence_after();
-              issue_s(x, j);
+              // S_X = Q_X K_j^T (K-major operands, LBO unused)
+              const uint32_t tS = tmem + C::TM_S + x * 128;
+              if constexpr (D == 128)
+                umma_ss_kmajor_x8(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
+              else
+                umma_ss_kmajor_x4(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
               umma_commit(bar(C::B_SFULL + x));
               if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
             }
           }
           // K_j's last reader is S_B,j (unpaired units only)
-          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + unit_of(k_unit(j))));
+          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + k_slot));
         }
-        n += (C::PAIRED ? 1 : 2) * sh.nkv;
         for (int x = 0; x < 2; ++x)
           if (nx[x] > 0) {
             ++nq[x];
