@@ -307,22 +307,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       Sched sch(n_qp, BH, CAUSAL);
       int bh, qp;
-      int nq[2] = {0, 0}, np[2] = {0, 0}, no[2] = {0, 0};  // Q_X items, P_X tiles, O_X items
+      // phase bits: P_X tiles (bit x), Q_X items (bit 2 + x), O_X items (bit
+      // 4 + x), and "tile X has finished an item" (bit 6 + x)
+      uint32_t ph = 0;
+      auto bit = [&](int b) { return (ph >> b) & 1u; };
       bool ok = true;
       // The ring units are consumed in index order (K_0 V_0 K_1 V_1 ..., or
       // one unit per key tile when paired), so a cursor (slot, phase) walks
       // them; the operand descriptors are fixed bases plus the slot offset
       // (shared-memory addresses stay below 2^18, so the 14-bit address field
       // of the descriptor cannot carry).
-      int cur_slot = 0;
-      uint32_t cur_phase = 0;
-      auto take = [&](int& slot, uint32_t& phase) {
-        slot = cur_slot;
-        phase = cur_phase;
-        if (++cur_slot == C::NUNIT) {
-          cur_slot = 0;
-          cur_phase ^= 1u;
-        }
+      // a ring position is 2 * slot + phase
+      uint32_t cur = 0;
+      auto take = [&](uint32_t& pos) {
+        pos = cur;
+        cur += 2;
+        if (cur == 2 * C::NUNIT) cur = 1;
+        else if (cur == 2 * C::NUNIT + 1) cur = 0;
       };
       // low 32 bits of a descriptor: start address >> 4 (bits 0-13) and
       // LBO >> 4 (bits 16-29); the high word (SBO = 1024, fixed bits) is the
@@ -333,71 +334,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_lo = ((sbase + C::Q_OFF) >> 4) | (1u << 16);
       constexpr uint32_t kUnitLo = C::UNIT_BYTES >> 4;
       constexpr uint32_t kVLo = ((C::PAIRED ? C::TILE_BYTES : 0) >> 4) | ((C::BLOCK_BYTES >> 4) << 16);
-      int k_slot = 0, v_slot = 0;  // ring slots of K_j and V_j-1 at this step
-      uint32_t k_phase = 0, v_phase = 0;
+      uint32_t kpos = 0, vpos = 0;  // ring positions of K_j and V_j-1 at this step
+      auto full_bar = [&](uint32_t pos) { return bar(C::B_FULL + static_cast<int>(pos >> 1)); };
+      auto next_units = [&](bool pv_step, bool s_step) {
+        // this step's units: V_j-1 (unpaired: its own unit; paired: the unit
+        // of K_j-1, taken at step j - 1), then K_j
+        if (pv_step) {
+          if constexpr (C::PAIRED)
+            vpos = kpos;
+          else
+            take(vpos);
+        }
+        if (s_step) take(kpos);
+      };
+      // O_X (+)= P_X V_j-1: V MN-major, LBO = next 64 columns of D, keys
+      // 64.. start 64 rows (8 KB) into each block
+      auto issue_pv = [&](int x, uint32_t acc) {
+        const uint32_t v_lo = ring_lo + (vpos >> 1) * kUnitLo + kVLo;
+        const uint32_t tO = tmem + C::TM_O + x * D, tP = tmem + C::TM_S + x * 128;
+        umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
+        umma_ts_mnmajor_x4(tO, tP + 32, desc(v_lo + (8192 >> 4)), idesc_o, 1u);
+      };
+      // S_X = Q_X K_j^T (K-major operands, LBO unused), then S_FULL[X]
+      auto issue_s = [&](int x) {
+        const uint32_t k_lo = ring_lo + (kpos >> 1) * kUnitLo + (1u << 16);
+        const uint32_t tS = tmem + C::TM_S + x * 128;
+        if constexpr (D == 128)
+          umma_ss_kmajor_x8(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
+        else
+          umma_ss_kmajor_x4(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
+        umma_commit(bar(C::B_SFULL + x));
+      };
       while (ok && sch.next(bh, qp)) {
         const ItemShape sh(qp, S, CAUSAL);
         const int nx[2] = {sh.nA, sh.nB};
         for (int x = 0; ok && x < 2; ++x)
-          if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), nq[x] & 1, wc, SITE_MMA_Q);
+          if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), bit(2 + x), wc, SITE_MMA_Q);
+        // steps 2 .. jf - 1 are interior for both tiles: every product is
+        // issued, and no item-boundary signal or wait falls on them
+        const int jf = min(nx[0], nx[1]) - 1;
         for (int j = 0; ok && j <= sh.nkv; ++j) {
-          const bool s_step = j < sh.nkv, pv_step = j >= 1;
-          // this step's units: V_j-1 (unpaired: its own unit; paired: the
-          // unit of K_j-1, taken at step j - 1), then K_j
-          if (pv_step) {
-            if constexpr (C::PAIRED) {
-              v_slot = k_slot;
-              v_phase = k_phase;
-            } else {
-              take(v_slot, v_phase);
+          if (j >= 2 && j < jf) {
+            // ---- steady step: one combined probe of the operands and P_A
+            next_units(true, true);
+            const uint32_t bv = full_bar(vpos), bk = full_bar(kpos), bpa = bar(C::B_PFULL);
+            if (!mbar_test3(bv, vpos & 1, bk, kpos & 1, bpa, bit(0))) {
+              ok = mbar_wait(bv, vpos & 1, wc, SITE_MMA_VFULL) &&
+                   mbar_wait(bk, kpos & 1, wc, SITE_MMA_KFULL) &&
+                   mbar_wait(bpa, bit(0), wc, SITE_MMA_PFULL);
+              if (!ok) break;
             }
+            tc_fence_after();
+            issue_pv(0, 1u);
+            issue_s(0);
+            ok = mbar_wait(bar(C::B_PFULL + 1), bit(1), wc, SITE_MMA_PFULL);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(1, 1u);
+            // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1)
+            umma_commit(bar(C::B_EMPTY + static_cast<int>(vpos >> 1)));
+            issue_s(1);
+            // K_j's last reader is S_B,j (unpaired units only)
+            if (!C::PAIRED) umma_commit(bar(C::B_EMPTY + static_cast<int>(kpos >> 1)));
+            ph ^= 3u;
+            continue;
           }
-          if (s_step) take(k_slot, k_phase);
+          // ---- general step (item start and end, ragged tiles)
+          const bool s_step = j < sh.nkv, pv_step = j >= 1;
+          next_units(pv_step, s_step);
           // the operand waits (normally met long before) come before the wait
           // for P; a paired unit was waited for when its K was needed
-          if (!C::PAIRED && pv_step) ok = mbar_wait(bar(C::B_FULL + v_slot), v_phase, wc, SITE_MMA_VFULL);
-          if (ok && s_step) ok = mbar_wait(bar(C::B_FULL + k_slot), k_phase, wc, SITE_MMA_KFULL);
-          const uint32_t k_lo = ring_lo + static_cast<uint32_t>(k_slot) * kUnitLo + (1u << 16);
-          const uint32_t v_lo = ring_lo + static_cast<uint32_t>(v_slot) * kUnitLo + kVLo;
+          if (!C::PAIRED && pv_step) ok = mbar_wait(full_bar(vpos), vpos & 1, wc, SITE_MMA_VFULL);
+          if (ok && s_step) ok = mbar_wait(full_bar(kpos), kpos & 1, wc, SITE_MMA_KFULL);
           for (int x = 0; ok && x < 2; ++x) {
             if (pv_step && j - 1 < nx[x]) {
-              ok = mbar_wait(bar(C::B_PFULL + x), np[x] & 1, wc, SITE_MMA_PFULL);
-              if (ok && j == 1 && no[x] >= 1)
-                ok = mbar_wait(bar(C::B_OFREE + x), (no[x] - 1) & 1, wc, SITE_MMA_OFREE);
+              ok = mbar_wait(bar(C::B_PFULL + x), bit(x), wc, SITE_MMA_PFULL);
+              // O_X was last read by the previous item's epilogue (O_X items
+              // parity flipped since, so the wanted phase is its complement)
+              if (ok && j == 1 && bit(6 + x))
+                ok = mbar_wait(bar(C::B_OFREE + x), bit(4 + x) ^ 1u, wc, SITE_MMA_OFREE);
               if (!ok) break;
               tc_fence_after();
-              // O_X (+)= P_X V_j-1: V MN-major, LBO = next 64 columns of D,
-              // keys 64.. start 64 rows (8 KB) into each block
-              const uint32_t tO = tmem + C::TM_O + x * D, tP = tmem + C::TM_S + x * 128;
-              const uint32_t acc = j > 1 ? 1u : 0u;
-              umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
-              umma_ts_mnmajor_x4(tO, tP + 32, desc(v_lo + (8192 >> 4)), idesc_o, 1u);
-              ++np[x];
+              issue_pv(x, j > 1 ? 1u : 0u);
+              ph ^= 1u << x;
               if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
-            // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1,
-            // whose S products came before)
-            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + v_slot));
+            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(vpos >> 1)));
             if (s_step && j < nx[x]) {
               tc_fence_after();
-              // S_X = Q_X K_j^T (K-major operands, LBO unused)
-              const uint32_t tS = tmem + C::TM_S + x * 128;
-              if constexpr (D == 128)
-                umma_ss_kmajor_x8(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
-              else
-                umma_ss_kmajor_x4(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
-              umma_commit(bar(C::B_SFULL + x));
+              issue_s(x);
               if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
             }
           }
-          // K_j's last reader is S_B,j (unpaired units only)
-          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + k_slot));
+          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(kpos >> 1)));
         }
         for (int x = 0; x < 2; ++x)
-          if (nx[x] > 0) {
-            ++nq[x];
-            ++no[x];
-          }
+          if (nx[x] > 0) ph = (ph ^ (0x14u << x)) | (0x40u << x);  // Q_X, O_X parity; item done
       }
       // every MMA issued completes before tensor memory is freed
       umma_commit(bar(C::B_DRAIN));
