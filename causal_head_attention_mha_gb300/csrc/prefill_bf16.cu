@@ -72,15 +72,23 @@ struct Cfg {
   static constexpr int BLOCK_BYTES = 128 * 128;   // one 128-row x 64-col bf16 block
   static constexpr int TILE_BYTES = KB * BLOCK_BYTES;
   // Ring of K/V units.  D = 64: a unit holds K_j and V_j of one key tile
-  // (one wait and one release per key step; 6 units leave ample lead).
-  // D = 128: a unit holds one K or one V tile (5 units; pairing them would
-  // leave only 2 units and too little lead for the loads).
+  // (one wait and one release per key step).  D = 128: a unit holds one K or
+  // one V tile (pairing them would leave only 2 units and too little lead
+  // for the loads).  5 units either way.
   static constexpr bool PAIRED = (D == 64);
-  static constexpr int NUNIT = PAIRED ? 6 : 5;
+  static constexpr int NUNIT = 5;
   static constexpr int UNIT_BYTES = (PAIRED ? 2 : 1) * TILE_BYTES;
+  // D = 64: the P V product has 16 more columns whose B operand is a fixed
+  // block (first column 1, the rest 0), so O_X column D accumulates the row's
+  // sum of bf16 weights -- the normaliser of O -- in the tensor core.  (At
+  // D = 128 tensor memory has no room for the wider O; the softmax threads
+  // add the rounded weights themselves.)
+  static constexpr bool ONES = (D == 64);
+  static constexpr int ON = D + (ONES ? 16 : 0);  // columns of the P V product
   static constexpr int Q_OFF = 0;                 // Q_A, Q_B
   static constexpr int RING_OFF = 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + NUNIT * UNIT_BYTES;
+  static constexpr int ONES_OFF = RING_OFF + NUNIT * UNIT_BYTES;  // 16 rows x 128 B
+  static constexpr int BAR_OFF = ONES_OFF + (ONES ? 2048 : 0);
   // barrier indices ([X] = one per query tile)
   static constexpr int B_QFULL = 0;               // [X] Q_X landed
   static constexpr int B_QEMPTY = 2;              // [X] the item's last S_X complete
@@ -94,11 +102,13 @@ struct Cfg {
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + flags, alignment slack
   // tensor-memory columns: S_A, S_B (128 fp32 columns each; P_X is written
-  // as bf16 pairs over the first 64 columns of S_X), then O_A, O_B
+  // as bf16 pairs over the first 64 columns of S_X), then O_A, O_B (ON
+  // columns each, O_STRIDE apart)
   static constexpr uint32_t TM_S = 0, TM_O = 256;
+  static constexpr uint32_t O_STRIDE = ONES ? 128 : D;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(NBAR * 8 + 8 <= 512, "barrier area");
-  static_assert(TM_O + 2 * D <= TM_COLS, "tensor memory");
+  static_assert(TM_O + O_STRIDE + ON <= TM_COLS, "tensor memory");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -218,6 +228,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (C::ONES) {
+    // the fixed block of the P V product: MN-major, 128-byte swizzle, 16
+    // key rows; element (row r, column 0) is 1 -- logical 16-byte chunk 0 of
+    // row r sits at physical chunk r % 8 -- and every other element is 0
+    if (threadIdx.x < 128) {
+      const int r = threadIdx.x >> 3, pc = threadIdx.x & 7;
+      const uint32_t w0 = (pc == (r & 7)) ? 0x3F80u : 0u;  // bf16 1.0 in the low half
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %2, %2};" ::"r"(
+                       sbase + C::ONES_OFF + static_cast<uint32_t>(threadIdx.x) * 16u),
+                   "r"(w0), "r"(0u)
+                   : "memory");
+      fence_proxy_async_smem();  // visible to the tensor core
+    }
+  }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), C::TM_COLS);
     tmem_relinquish();
@@ -304,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // it waits until the previous item's epilogue of tile X has read O_X.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, C::ON, true);
       Sched sch(n_qp, BH, CAUSAL);
       int bh, qp;
       // phase bits: P_X tiles (bit x), Q_X items (bit 2 + x), O_X items (bit
@@ -333,7 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring_lo = (sbase + C::RING_OFF) >> 4;
       const uint32_t q_lo = ((sbase + C::Q_OFF) >> 4) | (1u << 16);
       constexpr uint32_t kUnitLo = C::UNIT_BYTES >> 4;
-      constexpr uint32_t kVLo = ((C::PAIRED ? C::TILE_BYTES : 0) >> 4) | ((C::BLOCK_BYTES >> 4) << 16);
+      // V of slot s: start = ring + s * unit (+ K's tile when paired); LBO =
+      // the next 64 columns of V, or (ONES) the fixed block, which lies past
+      // every slot, so its distance shrinks by one unit per slot
+      constexpr uint32_t kVOff = (C::PAIRED ? C::TILE_BYTES : 0) >> 4;
+      constexpr uint32_t kVLbo0 = C::ONES ? ((C::ONES_OFF - C::RING_OFF) >> 4) - kVOff : (C::BLOCK_BYTES >> 4);
+      constexpr uint32_t kVLo = kVOff | (kVLbo0 << 16);
+      constexpr uint32_t kVSlot = C::ONES ? kUnitLo - (kUnitLo << 16) : kUnitLo;
+      // keys 64..127 of V start 64 rows (8 KB) further
+      constexpr uint32_t kVHalf = C::ONES ? 512u - (512u << 16) : 512u;
       uint32_t kpos = 0, vpos = 0;  // ring positions of K_j and V_j-1 at this step
       auto full_bar = [&](uint32_t pos) { return bar(C::B_FULL + static_cast<int>(pos >> 1)); };
       auto next_units = [&](bool pv_step, bool s_step) {
@@ -350,10 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_X (+)= P_X V_j-1: V MN-major, LBO = next 64 columns of D, keys
       // 64.. start 64 rows (8 KB) into each block
       auto issue_pv = [&](int x, uint32_t acc) {
-        const uint32_t v_lo = ring_lo + (vpos >> 1) * kUnitLo + kVLo;
-        const uint32_t tO = tmem + C::TM_O + x * D, tP = tmem + C::TM_S + x * 128;
-        umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
-        umma_ts_mnmajor_x4(tO, tP + 32, desc(v_lo + (8192 >> 4)), idesc_o, 1u);
+        const uint32_t v_lo = ring_lo + kVLo + (vpos >> 1) * kVSlot;
+        const uint32_t tO = tmem + C::TM_O + x * C::O_STRIDE, tP = tmem + C::TM_S + x * 128;
+        if constexpr (C::ONES) {
+          umma_ts_mnmajor_x4_b1fixed(tO, tP, desc(v_lo), idesc_o, acc);
+          umma_ts_mnmajor_x4_b1fixed(tO, tP + 32, desc(v_lo + kVHalf), idesc_o, 1u);
+        } else {
+          umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
+          umma_ts_mnmajor_x4(tO, tP + 32, desc(v_lo + kVHalf), idesc_o, 1u);
+        }
       };
       // S_X = Q_X K_j^T (K-major operands, LBO unused), then S_FULL[X]
       auto issue_s = [&](int x) {
@@ -446,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
-    const uint32_t tO = tmem + lane_base + C::TM_O + x * D;
+    const uint32_t tO = tmem + lane_base + C::TM_O + x * C::O_STRIDE;
     const uint32_t sfull = bar(C::B_SFULL + x), pfull = bar(C::B_PFULL + x);
     Sched sch(n_qp, BH, CAUSAL);
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
@@ -524,8 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
               pk[h][i] = pack_bf16x2(e.x, e.y);
               se[i & 3] = add2(se[i & 3], e);
-              sr[(i & 3) * 2] = add_bf16_lo(pk[h][i], sr[(i & 3) * 2]);
-              sr[(i & 3) * 2 + 1] = add_bf16_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+              if constexpr (!C::ONES) {
+                sr[(i & 3) * 2] = add_bf16_lo(pk[h][i], sr[(i & 3) * 2]);
+                sr[(i & 3) * 2 + 1] = add_bf16_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+              }
             }
           }
           se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
@@ -547,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the same thread), so O_X is final through tile j - 1 here.
           const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < (C::ON + 31) / 32; ++c) {  // with the weight-sum column
             uint32_t o[32];
             tmem_ld_32x32b_x32(tO + c * 32, o);
 #pragma unroll
@@ -571,7 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       failed = !__all_sync(0xffffffffu, mbar_wait(bar(C::B_OFULL + x), no & 1, wc, SITE_SM_OFULL));
       if (failed) break;
       tc_fence_after();
-      const float inv_lp = 1.0f / lp_run;
+      // O_X / (sum of the bf16 weights), from the tensor core's column D or
+      // from the softmax threads' own sum
+      float lp = lp_run;
+      if constexpr (C::ONES) {
+        uint32_t t[16];
+        tmem_ld_32x32b_x16(tO + D, t);
+        lp = __uint_as_float(t[0]);
+      }
+      const float inv_lp = 1.0f / lp;
       __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * S + q) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

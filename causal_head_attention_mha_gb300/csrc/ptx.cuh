@@ -341,6 +341,33 @@ __device__ __forceinline__ void umma_ts_mnmajor_x4(uint32_t d_tmem, uint32_t a_t
 }
 
 
+// The same 4 MMAs for an N = 80 product whose columns 64..79 come from one
+// fixed 16-row block: each MMA advances the start address by 16 rows and
+// lowers the leading-dimension offset (the distance to that block) by the
+// same amount, so every MMA reads the fixed block at the same place.
+__device__ __forceinline__ void umma_ts_mnmajor_x4_b1fixed(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t acc_first) {
+  asm volatile("{\n\t"
+               ".reg .pred pf, pt;\n\t"
+               ".reg .b64 b;\n\t"
+               ".reg .b32 a;\n\t"
+               "setp.ne.b32 pf, %4, 0;\n\t"
+               "setp.eq.b32 pt, %4, %4;\n\t"
+               "add.s64 b, %2, 0;\n\t"
+               "add.u32 a, %1, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pf;\n\t"
+               "add.s64 b, %2, -8388480;\n\t"
+               "add.u32 a, %1, 8;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+               "add.s64 b, %2, -16776960;\n\t"
+               "add.u32 a, %1, 16;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+               "add.s64 b, %2, -25165440;\n\t"
+               "add.u32 a, %1, 24;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+               "}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc_first) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
