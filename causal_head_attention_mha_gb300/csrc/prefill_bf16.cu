@@ -84,6 +84,11 @@ struct Cfg {
   // D = 128 tensor memory has no room for the wider O; the softmax threads
   // add the rounded weights themselves.)
   static constexpr bool ONES = (D == 64);
+  // D = 128: warp 3 vouches for each step's K and V units through "P_A
+  // ready", so the MMA thread checks no ring barrier in a steady step (two
+  // barrier checks fewer per step).  D = 64 needs one check (paired units),
+  // which the MMA thread probes together with P_A: measured faster there.
+  static constexpr bool WATCH = (D == 128);
   static constexpr int ON = D + (ONES ? 16 : 0);  // columns of the P V product
   static constexpr int Q_OFF = 0;                 // Q_A, Q_B
   static constexpr int RING_OFF = 2 * TILE_BYTES;
@@ -115,7 +120,30 @@ struct Cfg {
 // sites recorded with a timeout (bits 8.. of the error word)
 enum : uint32_t {
   SITE_PROD_EMPTY = 1, SITE_PROD_QEMPTY, SITE_MMA_Q, SITE_MMA_KFULL, SITE_MMA_VFULL,
-  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL
+  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL, SITE_WATCH_FULL, SITE_WATCH_PFULL
+};
+
+// The K/V units each key step reads, walked in the order the producer fills
+// the ring: V_j-1 (its own unit; paired: the unit of K_j-1), then K_j.  A
+// position is 2 * slot + phase.
+template <int NUNIT, bool PAIRED>
+struct RingWalk {
+  uint32_t cur = 0, kpos = 0, vpos = 0;
+  __device__ __forceinline__ void take(uint32_t& pos) {
+    pos = cur;
+    cur += 2;
+    if (cur == 2 * NUNIT) cur = 1;
+    else if (cur == 2 * NUNIT + 1) cur = 0;
+  }
+  __device__ __forceinline__ void step(bool pv_step, bool s_step) {
+    if (pv_step) {
+      if constexpr (PAIRED)
+        vpos = kpos;
+      else
+        take(vpos);
+    }
+    if (s_step) take(kpos);
+  }
 };
 
 // Key-tile counts of one item (query block qp of 256 rows).
@@ -216,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_QFULL + x), 1);
       mbar_init(bar(C::B_QEMPTY + x), 1);
       mbar_init(bar(C::B_SFULL + x), 1);
-      mbar_init(bar(C::B_PFULL + x), 128);
+      // tile A: one more arrival, from the operand watcher (warp 3)
+      mbar_init(bar(C::B_PFULL + x), (x == 0 && C::WATCH) ? 129 : 128);
       mbar_init(bar(C::B_OFULL + x), 1);
       mbar_init(bar(C::B_OFREE + x), 128);
     }
@@ -341,14 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // them; the operand descriptors are fixed bases plus the slot offset
       // (shared-memory addresses stay below 2^18, so the 14-bit address field
       // of the descriptor cannot carry).
-      // a ring position is 2 * slot + phase
-      uint32_t cur = 0;
-      auto take = [&](uint32_t& pos) {
-        pos = cur;
-        cur += 2;
-        if (cur == 2 * C::NUNIT) cur = 1;
-        else if (cur == 2 * C::NUNIT + 1) cur = 0;
-      };
+      RingWalk<C::NUNIT, C::PAIRED> ring;
       // low 32 bits of a descriptor: start address >> 4 (bits 0-13) and
       // LBO >> 4 (bits 16-29); the high word (SBO = 1024, fixed bits) is the
       // same for every operand here
@@ -366,23 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kVSlot = C::ONES ? kUnitLo - (kUnitLo << 16) : kUnitLo;
       // keys 64..127 of V start 64 rows (8 KB) further
       constexpr uint32_t kVHalf = C::ONES ? 512u - (512u << 16) : 512u;
-      uint32_t kpos = 0, vpos = 0;  // ring positions of K_j and V_j-1 at this step
       auto full_bar = [&](uint32_t pos) { return bar(C::B_FULL + static_cast<int>(pos >> 1)); };
-      auto next_units = [&](bool pv_step, bool s_step) {
-        // this step's units: V_j-1 (unpaired: its own unit; paired: the unit
-        // of K_j-1, taken at step j - 1), then K_j
-        if (pv_step) {
-          if constexpr (C::PAIRED)
-            vpos = kpos;
-          else
-            take(vpos);
-        }
-        if (s_step) take(kpos);
-      };
       // O_X (+)= P_X V_j-1: V MN-major, LBO = next 64 columns of D, keys
       // 64.. start 64 rows (8 KB) into each block
       auto issue_pv = [&](int x, uint32_t acc) {
-        const uint32_t v_lo = ring_lo + kVLo + (vpos >> 1) * kVSlot;
+        const uint32_t v_lo = ring_lo + kVLo + (ring.vpos >> 1) * kVSlot;
         const uint32_t tO = tmem + C::TM_O + x * C::O_STRIDE, tP = tmem + C::TM_S + x * 128;
         if constexpr (C::ONES) {
           umma_ts_mnmajor_x4_b1fixed(tO, tP, desc(v_lo), idesc_o, acc);
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // S_X = Q_X K_j^T (K-major operands, LBO unused), then S_FULL[X]
       auto issue_s = [&](int x) {
-        const uint32_t k_lo = ring_lo + (kpos >> 1) * kUnitLo + (1u << 16);
+        const uint32_t k_lo = ring_lo + (ring.kpos >> 1) * kUnitLo + (1u << 16);
         const uint32_t tS = tmem + C::TM_S + x * 128;
         if constexpr (D == 128)
           umma_ss_kmajor_x8(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
@@ -412,15 +422,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jf = min(nx[0], nx[1]) - 1;
         for (int j = 0; ok && j <= sh.nkv; ++j) {
           if (j >= 2 && j < jf) {
-            // ---- steady step: one combined probe of the operands and P_A
-            next_units(true, true);
-            const uint32_t bv = full_bar(vpos), bk = full_bar(kpos), bpa = bar(C::B_PFULL);
-            if (!mbar_test3(bv, vpos & 1, bk, kpos & 1, bpa, bit(0))) {
-              ok = mbar_wait(bv, vpos & 1, wc, SITE_MMA_VFULL) &&
-                   mbar_wait(bk, kpos & 1, wc, SITE_MMA_KFULL) &&
-                   mbar_wait(bpa, bit(0), wc, SITE_MMA_PFULL);
-              if (!ok) break;
+            // ---- steady step: "P_A ready" also says this step's K and V
+            // landed (the watcher's arrival)
+            ring.step(true, true);
+            if constexpr (C::WATCH) {
+              ok = mbar_wait(bar(C::B_PFULL), bit(0), wc, SITE_MMA_PFULL);
+            } else {
+              const uint32_t bv = full_bar(ring.vpos), bk = full_bar(ring.kpos), bpa = bar(C::B_PFULL);
+              if (!mbar_test3(bv, ring.vpos & 1, bk, ring.kpos & 1, bpa, bit(0)))
+                ok = mbar_wait(bv, ring.vpos & 1, wc, SITE_MMA_VFULL) &&
+                     mbar_wait(bk, ring.kpos & 1, wc, SITE_MMA_KFULL) &&
+                     mbar_wait(bpa, bit(0), wc, SITE_MMA_PFULL);
             }
+            if (!ok) break;
             tc_fence_after();
             issue_pv(0, 1u);
             issue_s(0);
@@ -429,20 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_pv(1, 1u);
             // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1)
-            umma_commit(bar(C::B_EMPTY + static_cast<int>(vpos >> 1)));
+            umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.vpos >> 1)));
             issue_s(1);
             // K_j's last reader is S_B,j (unpaired units only)
-            if (!C::PAIRED) umma_commit(bar(C::B_EMPTY + static_cast<int>(kpos >> 1)));
+            if (!C::PAIRED) umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.kpos >> 1)));
             ph ^= 3u;
             continue;
           }
           // ---- general step (item start and end, ragged tiles)
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
-          next_units(pv_step, s_step);
-          // the operand waits (normally met long before) come before the wait
-          // for P; a paired unit was waited for when its K was needed
-          if (!C::PAIRED && pv_step) ok = mbar_wait(full_bar(vpos), vpos & 1, wc, SITE_MMA_VFULL);
-          if (ok && s_step) ok = mbar_wait(full_bar(kpos), kpos & 1, wc, SITE_MMA_KFULL);
+          ring.step(pv_step, s_step);
+          // Operand waits, where "P_A ready" does not already cover them (no
+          // P_A V at this step); a paired unit was waited for when its K was
+          // needed
+          if (!C::WATCH || !(pv_step && j - 1 < nx[0])) {
+            if (!C::PAIRED && pv_step)
+              ok = mbar_wait(full_bar(ring.vpos), ring.vpos & 1, wc, SITE_MMA_VFULL);
+            if (ok && s_step) ok = mbar_wait(full_bar(ring.kpos), ring.kpos & 1, wc, SITE_MMA_KFULL);
+          }
           for (int x = 0; ok && x < 2; ++x) {
             if (pv_step && j - 1 < nx[x]) {
               ok = mbar_wait(bar(C::B_PFULL + x), bit(x), wc, SITE_MMA_PFULL);
@@ -456,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               ph ^= 1u << x;
               if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
-            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(vpos >> 1)));
+            if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.vpos >> 1)));
             if (s_step && j < nx[x]) {
               tc_fence_after();
               issue_s(x);
               if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
             }
           }
-          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(kpos >> 1)));
+          if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.kpos >> 1)));
         }
         for (int x = 0; x < 2; ++x)
           if (nx[x] > 0) ph = (ph ^ (0x14u << x)) | (0x40u << x);  // Q_X, O_X parity; item done
@@ -473,7 +491,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_DRAIN), 0, kDrainLimitNs);
     }
     __syncwarp();
-  }  // warp 3: no role
+  } else {
+    // ------------------------------------------------------------ operand watcher
+    // Every key step whose products include P_A,j-1 V_j-1 starts with the
+    // MMA thread's wait for "P_A ready".  This warp makes that one wait
+    // also cover the step's K and V units: it waits until they have landed
+    // and then adds its own arrival to that phase (which so needs 129), so
+    // the MMA thread checks no ring barrier in those steps.  It arrives for
+    // a phase only after the previous phase has completed.
+    if (C::WATCH && lane == 0) {
+      Sched sch(n_qp, BH, CAUSAL);
+      RingWalk<C::NUNIT, C::PAIRED> ring;
+      int bh, qp;
+      uint32_t pa = 0;  // phase parity of "P_A ready"
+      bool ok = true;
+      const uint32_t pfull_a = bar(C::B_PFULL);
+      while (ok && sch.next(bh, qp)) {
+        const ItemShape sh(qp, S, CAUSAL);
+        for (int j = 0; ok && j <= sh.nkv; ++j) {
+          const bool s_step = j < sh.nkv, pv_step = j >= 1;
+          ring.step(pv_step, s_step);
+          if (!(pv_step && j - 1 < sh.nA)) continue;
+          if (!C::PAIRED)
+            ok = mbar_wait(bar(C::B_FULL + static_cast<int>(ring.vpos >> 1)), ring.vpos & 1, wc,
+                           SITE_WATCH_FULL);
+          if (ok && s_step)
+            ok = mbar_wait(bar(C::B_FULL + static_cast<int>(ring.kpos >> 1)), ring.kpos & 1, wc,
+                           SITE_WATCH_FULL);
+          if (!ok) break;
+          mbar_arrive(pfull_a);
+          ok = mbar_wait(pfull_a, pa, wc, SITE_WATCH_PFULL);
+          pa ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax / epilogue
