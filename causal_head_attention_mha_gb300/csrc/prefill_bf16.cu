@@ -89,6 +89,7 @@ struct Cfg {
   // barrier checks fewer per step).  D = 64 needs one check (paired units),
   // which the MMA thread probes together with P_A: measured faster there.
   static constexpr bool WATCH = (D == 128);
+  static_assert(WATCH || PAIRED, "without the watcher, V shares K's unit (checked a step earlier)");
   static constexpr int ON = D + (ONES ? 16 : 0);  // columns of the P V product
   static constexpr int Q_OFF = 0;                 // Q_A, Q_B
   static constexpr int RING_OFF = 2 * TILE_BYTES;
@@ -428,10 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::WATCH) {
               ok = mbar_wait(bar(C::B_PFULL), bit(0), wc, SITE_MMA_PFULL);
             } else {
-              const uint32_t bv = full_bar(ring.vpos), bk = full_bar(ring.kpos), bpa = bar(C::B_PFULL);
-              if (!mbar_test3(bv, ring.vpos & 1, bk, ring.kpos & 1, bpa, bit(0)))
-                ok = mbar_wait(bv, ring.vpos & 1, wc, SITE_MMA_VFULL) &&
-                     mbar_wait(bk, ring.kpos & 1, wc, SITE_MMA_KFULL) &&
+              // paired units: V_j-1 shares the unit of K_j-1, checked at the
+              // previous step; K_j and P_A are probed together
+              const uint32_t bk = full_bar(ring.kpos), bpa = bar(C::B_PFULL);
+              if (!mbar_test2(bk, ring.kpos & 1, bpa, bit(0)))
+                ok = mbar_wait(bk, ring.kpos & 1, wc, SITE_MMA_KFULL) &&
                      mbar_wait(bpa, bit(0), wc, SITE_MMA_PFULL);
             }
             if (!ok) break;

@@ -85,23 +85,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
-// One non-blocking probe of three barrier phases at once: the three tests
-// are independent, so their latencies overlap.  True when all three phases
-// have completed (acquire, like a successful wait); false says nothing about
-// which one is missing.
-__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
-                                           uint32_t b2, uint32_t p2) {
+// One non-blocking probe of two barrier phases: true when both phases have
+// completed (acquire, like a successful wait); false says nothing about which
+// one is missing.
+__device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "{\n\t.reg .pred q0, q1;\n\t"
       "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
       "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
       "and.pred q0, q0, q1;\n\t"
-      "and.pred q0, q0, q2;\n\t"
       "selp.u32 %0, 1, 0, q0;\n\t}"
       : "=r"(ok)
-      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1)
       : "memory");
   return ok != 0;
 }
