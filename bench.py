@@ -44,10 +44,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # named workload, valid only while the kernel source hashes to the recorded value.
 TRAFFIC = {
     # profiles/prefill_bf16_d128_causal_b4h32s4096.md
-    "prefill": {"files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "d167eece1e8be2fb14b187ead9c4b133e14fd121dfde2e712255de406c471c50", "bytes_per_launch": 517964544},
+    "prefill": {"kernel": "prefill_bf16", "workload": PREFILL_WORKLOAD,
+                "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                "sha256": "137e9c8533c1bda16384bee0f29909909bca976f0ea31d6d4a6af384eaa87a39", "bytes_per_launch": 520408064},
+    # profiles/prefill_bf16_d64_causal_b2h16s16384.md
+    "prefill_d64": {"kernel": "prefill_bf16", "workload": "prefill_bf16_b2h16s16384d64",
+                    "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                    "sha256": "137e9c8533c1bda16384bee0f29909909bca976f0ea31d6d4a6af384eaa87a39", "bytes_per_launch": 251825664},
     # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
-    "decode": {"files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
+    "decode": {"kernel": "decode", "workload": DECODE_WORKLOAD, "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                "sha256": "cd2f0b5822aba3d400a9c178d01b3d3db17d173476f07ce74399531d28ca7f9c", "bytes_per_launch": 1201866048},
 }
 
@@ -60,11 +65,16 @@ def source_sha(rels):
     return h.hexdigest()
 
 
-def traffic_for(kernel):
-    t = TRAFFIC[kernel]
-    if t["sha256"] is None or t["bytes_per_launch"] is None:
-        return None
-    return t["bytes_per_launch"] if source_sha(t["files"]) == t["sha256"] else None
+def traffic_for(kernel, workload):
+    """Recorded DRAM bytes per launch of `kernel` on `workload`, or None when no
+    capture of this workload exists or the source changed since it was taken."""
+    for t in TRAFFIC.values():
+        if t["kernel"] != kernel or t["workload"] != workload:
+            continue
+        if t["sha256"] is None or t["bytes_per_launch"] is None:
+            return None
+        return t["bytes_per_launch"] if source_sha(t["files"]) == t["sha256"] else None
+    return None
 
 
 def load_peaks():
@@ -382,8 +392,7 @@ def run_ours(args, rank, world, dist):
                                 "qk_std": wp["qk_std"], "flops_per_step": flops}})
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    # the recorded counters belong to the default workload only
-                    "traffic": traffic_for("prefill") if args.prefill_workload == PREFILL_WORKLOAD else None,
+                    "traffic": traffic_for("prefill_bf16", args.prefill_workload),
                     "peak_source": f"bf16_tflops (burst), of {peak_src}",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                     "kernel": f"prefill_bf16_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
@@ -396,7 +405,7 @@ def run_ours(args, rank, world, dist):
         line["decode"] = {"value": gbs, "unit": "GB/s", "bound": "hbm",
                           "achieved": dbytes / (td / K_) / 1e9, "peak": peaks["hbm_gbs"],
                           "frac": dbytes / (td / K_) / 1e9 / peaks["hbm_gbs"],
-                          "traffic": traffic_for("decode"), "peak_source": f"hbm_gbs, of {peak_src}",
+                          "traffic": traffic_for("decode", DECODE_WORKLOAD), "peak_source": f"hbm_gbs, of {peak_src}",
                           "us_per_call": 1e6 * td / K_}
         if not do_prefill:
             line.update({"value": gbs, "unit": "GB/s"})
