@@ -249,35 +249,40 @@ def run_ours(args, rank, world, dist):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream(dev)
 
-    def bf16_dev(t):
-        return torch.from_numpy(t.bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    torch_dtype = {"bf16": torch.bfloat16, "f16": torch.float16}
+
+    def dev16(t, dtype):
+        return torch.from_numpy(t.bits.view(np.int16)).view(torch_dtype[dtype]).to(dev)
 
     do_prefill = args.only in ("both", "prefill")
     do_decode = args.only in ("both", "decode")
     wp = si.WORKLOADS[args.prefill_workload]
-    wd = si.WORKLOADS[DECODE_WORKLOAD]
+    wd = si.WORKLOADS[args.decode_workload]
+    pdt, ddt = wp["dtype"], wd.get("dtype", "bf16")
+    fwd = mha.mha_fwd_f16 if pdt == "f16" else mha.mha_fwd
+    dec = mha.mha_decode_f16 if ddt == "f16" else mha.mha_decode
     # each rank works on its own batch (weak scaling, no collective on the data path)
     if do_prefill:
         xp = si.prefill_inputs(wp["B"], wp["H"], wp["S"], wp["D"], rank_seed(wp["seed"], rank),
-                               qk_std=wp["qk_std"])
-        Q, K, V = bf16_dev(xp.Q), bf16_dev(xp.K), bf16_dev(xp.V)
+                               qk_std=wp["qk_std"], dtype=pdt)
+        Q, K, V = dev16(xp.Q, pdt), dev16(xp.K, pdt), dev16(xp.V, pdt)
         O = torch.empty_like(Q)
         LSE = torch.empty((xp.B, xp.H, xp.S), dtype=torch.float32, device=dev)
         flops = prefill_flops(xp.B, xp.H, xp.S, xp.D, True)
     if do_decode:
         xd = si.decode_inputs(wd["B"], wd["H"], wd["D"], rank_seed(wd["seed"], rank), wd["len_lo"],
-                              wd["len_hi"])
-        q, Kc, Vc = bf16_dev(xd.q), bf16_dev(xd.Kc), bf16_dev(xd.Vc)
+                              wd["len_hi"], dtype=ddt)
+        q, Kc, Vc = dev16(xd.q, ddt), dev16(xd.Kc, ddt), dev16(xd.Vc, ddt)
         sl = torch.from_numpy(xd.seqlens).to(dev)
         Od = torch.empty_like(q)
         dbytes = decode_bytes(xd.B, xd.H, xd.D, xd.seqlens)
         nsplit = mha.mha_decode_num_splits(xd.B, xd.H)
 
     def prefill():
-        mha.mha_fwd(Q, K, V, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
+        fwd(Q, K, V, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
 
     def decode():
-        mha.mha_decode(q, Kc, Vc, sl, O=Od, scale=xd.scale, stream=stream)
+        dec(q, Kc, Vc, sl, O=Od, scale=xd.scale, stream=stream)
 
     def barrier():
         if dist is not None:
@@ -381,7 +386,7 @@ def run_ours(args, rank, world, dist):
         return 0
 
     line = {"impl": "ours", "metric": METRIC}
-    cfg = {"workload": args.prefill_workload if do_prefill else DECODE_WORKLOAD,
+    cfg = {"workload": args.prefill_workload if do_prefill else args.decode_workload,
            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
     if do_prefill:
         value = whole_job_rate(world, K_ * flops, tp) / 1e12
@@ -392,10 +397,10 @@ def run_ours(args, rank, world, dist):
                                 "qk_std": wp["qk_std"], "flops_per_step": flops}})
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "traffic": traffic_for("prefill_bf16", args.prefill_workload),
+                    "traffic": traffic_for("prefill_" + pdt, args.prefill_workload),
                     "peak_source": f"bf16_tflops (burst), of {peak_src}",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "kernel": f"prefill_bf16_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
+                    "kernel": f"prefill_{pdt}_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
         line["roofline"] = roofline
     if do_decode:
         gbs = whole_job_rate(world, K_ * dbytes, td) / 1e9
@@ -405,13 +410,14 @@ def run_ours(args, rank, world, dist):
         line["decode"] = {"value": gbs, "unit": "GB/s", "bound": "hbm",
                           "achieved": dbytes / (td / K_) / 1e9, "peak": peaks["hbm_gbs"],
                           "frac": dbytes / (td / K_) / 1e9 / peaks["hbm_gbs"],
-                          "traffic": traffic_for("decode", DECODE_WORKLOAD), "peak_source": f"hbm_gbs, of {peak_src}",
+                          "traffic": traffic_for("decode", args.decode_workload), "peak_source": f"hbm_gbs, of {peak_src}",
                           "us_per_call": 1e6 * td / K_}
         if not do_prefill:
             line.update({"value": gbs, "unit": "GB/s"})
     line.update({
         "n_gpus": world, "steps": K_, "warmup": args.warmup, "ms_per_step": 1e3 * total / K_,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": pdt if do_prefill else ddt,
         "data": "synthetic", "config": cfg, "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches,
     })
@@ -430,8 +436,11 @@ def main():
     ap.add_argument("--only", choices=("both", "prefill", "decode"), default="both")
     ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
                     choices=[k for k, w in si.WORKLOADS.items()
-                             if w["kind"] == "prefill" and w["dtype"] == "bf16"],
-                    help="bf16 prefill workload of the step (default: the headline one)")
+                             if w["kind"] == "prefill" and w["dtype"] in ("bf16", "f16")],
+                    help="prefill workload of the step, bf16 or f16 (default: the headline one)")
+    ap.add_argument("--decode-workload", default=DECODE_WORKLOAD,
+                    choices=[k for k, w in si.WORKLOADS.items() if w["kind"] == "decode"],
+                    help="decode workload of the step (bf16 or f16)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -43,10 +43,14 @@ def _declare(lib):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.mha_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.mha_fwd.restype = i
+    lib.mha_fwd_f16.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.mha_fwd_f16.restype = i
     lib.mha_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.mha_fwd_f32.restype = i
     lib.mha_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
     lib.mha_decode.restype = i
+    lib.mha_decode_f16.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
+    lib.mha_decode_f16.restype = i
     lib.mha_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
     lib.mha_decode_noalloc.restype = i
     lib.mha_decode_num_splits.argtypes = [i, i]
@@ -131,10 +135,40 @@ def mha_fwd(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, wan
     return _prefill("mha_fwd", torch.bfloat16, Q, K, V, O, LSE, scale, causal, stream, want_lse)
 
 
+def mha_fwd_f16(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, want_lse=True):
+    """f16 [B,H,S,D] prefill; returns (O, LSE).  See include/mha.h: mha_fwd_f16."""
+    return _prefill("mha_fwd_f16", torch.float16, Q, K, V, O, LSE, scale, causal, stream,
+                    want_lse)
+
+
 def mha_fwd_f32(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, want_lse=True):
     """float32 [B,H,S,D] prefill; returns (O, LSE).  See include/mha.h: mha_fwd_f32."""
     return _prefill("mha_fwd_f32", torch.float32, Q, K, V, O, LSE, scale, causal, stream,
                     want_lse)
+
+
+def _decode(entry, dtype, q, Kcache, Vcache, seqlens, O, scale, stream):
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, D]")
+    B, H, D = q.shape
+    dev = q.device
+    _check(q, "q", dtype, (B, H, D), dev)
+    if Kcache.dim() != 3 or Kcache.shape[1:] != (H, D):
+        raise ValueError("Kcache must be [total_tokens, H, D]")
+    _check(Kcache, "Kcache", dtype, tuple(Kcache.shape), dev)
+    _check(Vcache, "Vcache", dtype, tuple(Kcache.shape), dev)
+    _check(seqlens, "seqlens", torch.int32, (B,), dev)
+    if O is None:
+        O = torch.empty_like(q)
+    _check(O, "O", dtype, (B, H, D), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = getattr(_load(), entry)(q.data_ptr(), Kcache.data_ptr(), Vcache.data_ptr(),
+                                 seqlens.data_ptr(), O.data_ptr(), B, H, D, float(scale),
+                                 _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, entry)
+    return O
 
 
 def mha_decode(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
@@ -142,26 +176,12 @@ def mha_decode(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
 
     q: [B,H,D]; Kcache, Vcache: [sum(seqlens), H, D]; seqlens: int32 [B] on the device.
     """
-    if q.dim() != 3:
-        raise ValueError("q must be [B, H, D]")
-    B, H, D = q.shape
-    dev = q.device
-    _check(q, "q", torch.bfloat16, (B, H, D), dev)
-    if Kcache.dim() != 3 or Kcache.shape[1:] != (H, D):
-        raise ValueError("Kcache must be [total_tokens, H, D]")
-    _check(Kcache, "Kcache", torch.bfloat16, tuple(Kcache.shape), dev)
-    _check(Vcache, "Vcache", torch.bfloat16, tuple(Kcache.shape), dev)
-    _check(seqlens, "seqlens", torch.int32, (B,), dev)
-    if O is None:
-        O = torch.empty_like(q)
-    _check(O, "O", torch.bfloat16, (B, H, D), dev)
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
-    st = _load().mha_decode(q.data_ptr(), Kcache.data_ptr(), Vcache.data_ptr(), seqlens.data_ptr(),
-                            O.data_ptr(), B, H, D, float(scale), _stream_ptr(stream, dev))
-    if st != MHA_OK:
-        raise MHAError(st, "mha_decode")
-    return O
+    return _decode("mha_decode", torch.bfloat16, q, Kcache, Vcache, seqlens, O, scale, stream)
+
+
+def mha_decode_f16(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
+    """mha_decode on f16 q, cache and O.  See include/mha.h: mha_decode_f16."""
+    return _decode("mha_decode_f16", torch.float16, q, Kcache, Vcache, seqlens, O, scale, stream)
 
 
 def mha_decode_noalloc(q, Kcache, Vcache, seqlens, O, scale=None, stream=None):

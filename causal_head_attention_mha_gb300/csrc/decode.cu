@@ -21,6 +21,7 @@
 // first (longest-processing-time order computed on the device).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "launch.h"
 
@@ -39,8 +40,30 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return r;
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// The 16-bit element type of q, the cache and O: widening of a packed pair
+// to float (exact) and rounding of a float result (to nearest even).
+template <bool F16>
+struct Elem;
+template <>
+struct Elem<false> {  // bf16
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+  static __device__ __forceinline__ uint16_t round(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+};
+template <>
+struct Elem<true> {  // f16
+  static __device__ __forceinline__ float lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+  }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  }
+  static __device__ __forceinline__ uint16_t round(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+  }
+};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -48,11 +71,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ Kc,
-    const __nv_bfloat16* __restrict__ Vc, const int* __restrict__ seqlens, float* __restrict__ ws,
-    __nv_bfloat16* __restrict__ O, int B, int H, int nsplit, float c_log2) {
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ Kc,
+    const uint16_t* __restrict__ Vc, const int* __restrict__ seqlens, float* __restrict__ ws,
+    uint16_t* __restrict__ O, int B, int H, int nsplit, float c_log2) {
+  using E = Elem<F16>;
   constexpr int LPK = D / 8;      // lanes per key row
   constexpr int KPW = 32 / LPK;   // keys per warp step
   constexpr int NG = NW * KPW;    // lane groups per CTA
@@ -108,8 +132,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
     const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      qf[2 * e] = bf16lo(w[e]) * c_log2;
-      qf[2 * e + 1] = bf16hi(w[e]) * c_log2;
+      qf[2 * e] = E::lo(w[e]) * c_log2;
+      qf[2 * e + 1] = E::hi(w[e]) * c_log2;
     }
   }
   float m = -INFINITY, l = 0.f, acc[8];
@@ -117,8 +141,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 
   const size_t row_stride = static_cast<size_t>(H) * D;  // elements between consecutive tokens
-  const __nv_bfloat16* kbase = Kc + (static_cast<size_t>(off) * H + h) * D + sub * 8;
-  const __nv_bfloat16* vbase = Vc + (static_cast<size_t>(off) * H + h) * D + sub * 8;
+  const uint16_t* kbase = Kc + (static_cast<size_t>(off) * H + h) * D + sub * 8;
+  const uint16_t* vbase = Vc + (static_cast<size_t>(off) * H + h) * D + sub * 8;
 
   for (int tw = t0 + warp * KPW; tw < t1; tw += STEP * U) {
     uint4 kr[U], vr[U];
@@ -142,8 +166,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
       float s = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        s = fmaf(qf[2 * e], bf16lo(w[e]), s);
-        s = fmaf(qf[2 * e + 1], bf16hi(w[e]), s);
+        s = fmaf(qf[2 * e], E::lo(w[e]), s);
+        s = fmaf(qf[2 * e + 1], E::hi(w[e]), s);
       }
 #pragma unroll
       for (int o = LPK / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -165,8 +189,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
         const uint32_t w[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          acc[2 * e] = fmaf(p, bf16lo(w[e]), acc[2 * e]);
-          acc[2 * e + 1] = fmaf(p, bf16hi(w[e]), acc[2 * e + 1]);
+          acc[2 * e] = fmaf(p, E::lo(w[e]), acc[2 * e]);
+          acc[2 * e + 1] = fmaf(p, E::hi(w[e]), acc[2 * e + 1]);
         }
       }
       m = m_new;
@@ -196,7 +220,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
       }
     }
     if (nsplit == 1) {
-      O[bh * D + d] = __float2bfloat16_rn(Ls > 0.f ? o / Ls : 0.f);
+      O[bh * D + d] = E::round(Ls > 0.f ? o / Ls : 0.f);
     } else {
       float* part = ws + (bh * nsplit + split) * (D + 2);
       part[d] = o;
@@ -209,9 +233,9 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(
 }
 
 // One CTA per (h, b): merge the nsplit partials of that row.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict__ ws,
-                                                         __nv_bfloat16* __restrict__ O, int H,
+                                                         uint16_t* __restrict__ O, int H,
                                                          int nsplit) {
   const size_t bh = static_cast<size_t>(blockIdx.y) * H + blockIdx.x;
   const float* part = ws + bh * nsplit * (D + 2);
@@ -227,21 +251,21 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict
       o = fmaf(part[s * (D + 2) + d], w, o);
     }
   }
-  O[bh * D + d] = __float2bfloat16_rn(Ls > 0.f ? o / Ls : 0.f);
+  O[bh * D + d] = Elem<F16>::round(Ls > 0.f ? o / Ls : 0.f);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_t(const void* q, const void* Kc, const void* Vc, const int* seqlens, void* O,
                      float* ws, int B, int H, int nsplit, float c_log2, cudaStream_t stream) {
   dim3 grid(nsplit, H, B);
-  decode_split_kernel<D><<<grid, NW * 32, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(Kc),
-      static_cast<const __nv_bfloat16*>(Vc), seqlens, ws, static_cast<__nv_bfloat16*>(O), B, H,
-      nsplit, c_log2);
+  decode_split_kernel<D, F16><<<grid, NW * 32, 0, stream>>>(
+      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(Kc),
+      static_cast<const uint16_t*>(Vc), seqlens, ws, static_cast<uint16_t*>(O), B, H, nsplit,
+      c_log2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nsplit == 1) return e;
-  decode_merge_kernel<D><<<dim3(H, B), D, 0, stream>>>(ws, static_cast<__nv_bfloat16*>(O), H,
-                                                       nsplit);
+  decode_merge_kernel<D, F16><<<dim3(H, B), D, 0, stream>>>(ws, static_cast<uint16_t*>(O), H,
+                                                            nsplit);
   return cudaGetLastError();
 }
 
@@ -259,10 +283,14 @@ int decode_num_splits(int B, int H, int num_sms) {
 
 cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, const int* seqlens,
                           void* O, float* ws, int B, int H, int D, int nsplit, float scale,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool f16) {
   const float c_log2 = scale * 1.44269504088896340736f;
-  if (D == 128) return launch_t<128>(q, Kc, Vc, seqlens, O, ws, B, H, nsplit, c_log2, stream);
-  return launch_t<64>(q, Kc, Vc, seqlens, O, ws, B, H, nsplit, c_log2, stream);
+  if (f16) {
+    if (D == 128) return launch_t<128, true>(q, Kc, Vc, seqlens, O, ws, B, H, nsplit, c_log2, stream);
+    return launch_t<64, true>(q, Kc, Vc, seqlens, O, ws, B, H, nsplit, c_log2, stream);
+  }
+  if (D == 128) return launch_t<128, false>(q, Kc, Vc, seqlens, O, ws, B, H, nsplit, c_log2, stream);
+  return launch_t<64, false>(q, Kc, Vc, seqlens, O, ws, B, H, nsplit, c_log2, stream);
 }
 
 }  // namespace mha

@@ -78,6 +78,6 @@ extern "C" int mha_decode_noalloc(const void* q, const void* Kcache, const void*
     if (e != cudaSuccess) return mha::record_cuda_failure(e);
   }
   const cudaError_t e = mha::launch_decode(q, Kcache, Vcache, seqlens, O, ws, B, H, D, nsplit,
-                                           scale, static_cast<cudaStream_t>(stream));
+                                           scale, static_cast<cudaStream_t>(stream), false);
   return e == cudaSuccess ? MHA_OK : mha::record_cuda_failure(e);
 }

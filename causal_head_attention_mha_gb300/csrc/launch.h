@@ -14,6 +14,11 @@ cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, voi
                                 int B, int H, int S, int D, float scale, int causal,
                                 cudaStream_t stream, uint64_t wait_limit_ns, int inject);
 
+// The same on f16 inputs and outputs (P rounded to f16).
+cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int S, int D, float scale, int causal,
+                               cudaStream_t stream, uint64_t wait_limit_ns, int inject);
+
 cudaError_t launch_prefill_f32(const float* Q, const float* K, const float* V, float* O,
                                float* LSE, int B, int H, int S, int D, float scale, int causal,
                                cudaStream_t stream);
@@ -22,9 +27,10 @@ cudaError_t launch_prefill_f32(const float* Q, const float* K, const float* V, f
 int decode_num_splits(int B, int H, int num_sms);
 
 // Partials of the key splits go to `ws` (B*H*nsplit*(D+2) floats, ignored when nsplit == 1).
+// q, the cache and O are bf16, or f16 when `f16` is set.
 cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, const int* seqlens,
                           void* O, float* ws, int B, int H, int D, int nsplit, float scale,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool f16);
 
 // Reads and clears the device error word of the prefill translation unit.
 cudaError_t take_prefill_bf16_error(unsigned int* word);

@@ -70,6 +70,17 @@ int mha_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, in
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
 }
 
+int mha_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                int S, int D, float scale, int causal, void* stream) {
+  const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
+  if (st != MHA_OK) return st;
+  const cudaError_t e =
+      mha::launch_prefill_f16(Q, K, V, O, LSE, B, H, S, D, scale, causal,
+                              static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
+                              g_fault_injection.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
 int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE, int B,
                 int H, int S, int D, float scale, int causal, void* stream) {
   const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
@@ -79,8 +90,12 @@ int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float*
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
 }
 
-int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int* seqlens, void* O,
-               int B, int H, int D, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int decode_impl(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
+                void* O, int B, int H, int D, float scale, void* stream, bool f16) {
   if (!q || !Kcache || !Vcache || !seqlens || !O) return MHA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || D < 1) return MHA_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || scale == INFINITY) return MHA_ERR_INVALID_ARG;
@@ -100,12 +115,27 @@ int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int*
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  cudaError_t e = mha::launch_decode(q, Kcache, Vcache, seqlens, O, ws, B, H, D, nsplit, scale, s);
+  cudaError_t e =
+      mha::launch_decode(q, Kcache, Vcache, seqlens, O, ws, B, H, D, nsplit, scale, s, f16);
   if (ws) {
     const cudaError_t ef = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = ef;
   }
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int* seqlens, void* O,
+               int B, int H, int D, float scale, void* stream) {
+  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, false);
+}
+
+int mha_decode_f16(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
+                   void* O, int B, int H, int D, float scale, void* stream) {
+  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, true);
 }
 
 int mha_decode_num_splits(int B, int H) {

@@ -53,9 +53,6 @@ namespace {
 constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per tile
 constexpr float kLn2 = 0.69314718055994530942f;
-// Largest fp32 weight sum of one tile kept without moving the reference
-// maximum (2^64): every weight is then <= 2^64, far inside fp32 and bf16 range.
-constexpr float kMaxTileWeight = 18446744073709551616.0f;
 constexpr int kSoftmaxWarp0 = 4;  // warps 4..7: tile A, 8..11: tile B
 constexpr int kQWarp = 2;         // TMA producer of the Q tiles
 constexpr int kThreads = 384;     // three warpgroups: control, softmax A, softmax B
@@ -218,14 +215,41 @@ __device__ __forceinline__ void drain_ring(uint32_t full0, int nst, int issued) 
   }
 }
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
-                        const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                        float* __restrict__ lse, int S, int BH, float c_log2,
-                        uint64_t wait_limit_ns, int inject) {
+// The 16-bit type of Q, K, V, O and of the probabilities P (both operands of
+// one kind::f16 product have the same type, so P takes the inputs' type).
+template <bool F16>
+struct Elem;
+template <>
+struct Elem<false> {  // bf16
+  static constexpr uint32_t kOne = 0x3F80u;  // 1.0
+  // Largest fp32 weight sum of one tile kept without moving the reference
+  // maximum (2^64): every weight is then <= 2^64, far inside fp32 and bf16 range.
+  static constexpr float kMaxTileWeight = 18446744073709551616.0f;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  static __device__ __forceinline__ float add_lo(uint32_t w, float a) { return add_bf16_lo(w, a); }
+  static __device__ __forceinline__ float add_hi(uint32_t w, float a) { return add_bf16_hi(w, a); }
+};
+template <>
+struct Elem<true> {  // f16
+  static constexpr uint32_t kOne = 0x3C00u;  // 1.0
+  // f16 ends at 65504, so weights must stay <= 2^15.  With a 15 (log2) jump
+  // of the scores within reach on large logits, the f16 path takes every
+  // tile's row maximum first and moves the reference only when that maximum
+  // passes it by more than kHeadroom: every weight is then <= 2^15 before
+  // any exponential, and no tile is ever redone.
+  static constexpr float kHeadroom = 15.0f;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
+  static __device__ __forceinline__ float add_lo(uint32_t w, float a) { return add_f16_lo(w, a); }
+  static __device__ __forceinline__ float add_hi(uint32_t w, float a) { return add_f16_hi(w, a); }
+};
+
+template <int D, bool CAUSAL, bool F16>
+__device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                             const CUtensorMap& tmV, uint16_t* __restrict__ O,
+                                             float* __restrict__ lse, int S, int BH, float c_log2,
+                                             uint64_t wait_limit_ns, int inject) {
   using C = Cfg<D>;
+  using E = Elem<F16>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -264,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // row r sits at physical chunk r % 8 -- and every other element is 0
     if (threadIdx.x < 128) {
       const int r = threadIdx.x >> 3, pc = threadIdx.x & 7;
-      const uint32_t w0 = (pc == (r & 7)) ? 0x3F80u : 0u;  // bf16 1.0 in the low half
+      const uint32_t w0 = (pc == (r & 7)) ? E::kOne : 0u;  // 1.0 in the low half
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %2, %2};" ::"r"(
                        sbase + C::ONES_OFF + static_cast<uint32_t>(threadIdx.x) * 16u),
                    "r"(w0), "r"(0u)
@@ -357,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // P_X V signals O_FULL[X].  The first P_X V of an item overwrites O_X, so
     // it waits until the previous item's epilogue of tile X has read O_X.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, C::ON, true);
+      constexpr uint32_t idesc_s = idesc_f32acc(128, BN, false, F16);
+      constexpr uint32_t idesc_o = idesc_f32acc(128, C::ON, true, F16);
       Sched sch(n_qp, BH, CAUSAL);
       int bh, qp;
       // phase bits: P_X tiles (bit x), Q_X items (bit 2 + x), O_X items (bit
@@ -588,9 +612,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // common case.  Softmax does not depend on the reference, so this is
         // exact arithmetic.  A tile that does overflow (its scores exceed the
         // reference by ~64, log2 units) is redone from tensor memory with its
-        // true maximum, and O is rescaled.
+        // true maximum, and O is rescaled.  (That is the bf16 path; the f16
+        // path, whose weights must stay <= 2^15, takes every tile's row
+        // maximum instead: see Elem<true>.)
         const bool first = (j == 0);
         float m_use = first ? row_max(s) : m_run;
+        if constexpr (F16) {
+          if (!first) {
+            const float mx = row_max(s);
+            if (mx > m_run + E::kHeadroom) m_use = mx;
+          }
+        }
         const float2 c2 = make_float2(c_log2, c_log2);
         // P_X,j and its partial sums: the fp32 weights (for the log-sum-exp and
         // the overflow check) and the bf16-rounded weights the P.V product uses
@@ -614,18 +646,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
                                     c2, nm2);
               const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
-              pk[h][i] = pack_bf16x2(e.x, e.y);
+              pk[h][i] = E::pack(e.x, e.y);
               se[i & 3] = add2(se[i & 3], e);
               if constexpr (!C::ONES) {
-                sr[(i & 3) * 2] = add_bf16_lo(pk[h][i], sr[(i & 3) * 2]);
-                sr[(i & 3) * 2 + 1] = add_bf16_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+                sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
+                sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
               }
             }
           }
           se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
           rs = se[0].x + se[0].y;
           rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
-          const bool redo = pass == 0 && !first && !(rs <= kMaxTileWeight);  // also NaN / inf
+          bool redo = false;
+          if constexpr (!F16) redo = pass == 0 && !first && !(rs <= E::kMaxTileWeight);  // also NaN / inf
           if (!__any_sync(0xffffffffu, redo)) break;
           // rare: the scores are still in tensor memory (P is stored below)
           tmem_ld_32x32b_x128(tS, s);
@@ -674,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lp = __uint_as_float(t[0]);
       }
       const float inv_lp = 1.0f / lp;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * S + q) * D;
+      uint16_t* orow = O + (static_cast<size_t>(bh) * S + q) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -682,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_lp, __uint_as_float(o[2 * i + 1]) * inv_lp);
+          w[i] = E::pack(__uint_as_float(o[2 * i]) * inv_lp, __uint_as_float(o[2 * i + 1]) * inv_lp);
         if (q < S) {
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
@@ -705,6 +738,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The kernels: one per 16-bit input type, the same body.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
+                        float* __restrict__ lse, int S, int BH, float c_log2,
+                        uint64_t wait_limit_ns, int inject) {
+  prefill_body<D, CAUSAL, false>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, wait_limit_ns, inject);
+}
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_f16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
+                       float* __restrict__ lse, int S, int BH, float c_log2,
+                       uint64_t wait_limit_ns, int inject) {
+  prefill_body<D, CAUSAL, true>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, wait_limit_ns, inject);
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -724,8 +777,9 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [BH, S, D] bf16 viewed as a 3-D tensor (D innermost); box = 64 columns x 128 rows.
-bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D) {
+// [BH, S, D] 16-bit elements viewed as a 3-D tensor (D innermost); box = 64
+// columns x 128 rows.
+bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D, bool f16) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
@@ -733,18 +787,19 @@ bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D) {
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                     __nv_bfloat16* O, float* lse, int BH, int S, float c_log2,
+                     uint16_t* O, float* lse, int BH, int S, float c_log2,
                      cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
-  auto kern = prefill_bf16_kernel<D, CAUSAL>;
+  auto kern = F16 ? prefill_f16_kernel<D, CAUSAL> : prefill_bf16_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // The softmax warpgroups raise their register limit with registers the
@@ -763,23 +818,38 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   return cudaGetLastError();
 }
 
+template <bool F16>
+cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                           int B, int H, int S, int D, float scale, int causal,
+                           cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if (!encode_bhsd(&mq, Q, BH, S, D, F16) || !encode_bhsd(&mk, K, BH, S, D, F16) ||
+      !encode_bhsd(&mv, V, BH, S, D, F16))
+    return cudaErrorInvalidValue;
+  const float c_log2 = scale * 1.44269504088896340736f;  // scale * log2(e)
+  uint16_t* o = static_cast<uint16_t*>(O);
+  if (D == 128)
+    return causal ? launch_t<128, true, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject)
+                  : launch_t<128, false, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject);
+  return causal ? launch_t<64, true, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject)
+                : launch_t<64, false, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 int B, int H, int S, int D, float scale, int causal,
                                 cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
-  const int BH = B * H;
-  CUtensorMap mq, mk, mv;
-  if (!encode_bhsd(&mq, Q, BH, S, D) || !encode_bhsd(&mk, K, BH, S, D) ||
-      !encode_bhsd(&mv, V, BH, S, D))
-    return cudaErrorInvalidValue;
-  const float c_log2 = scale * 1.44269504088896340736f;  // scale * log2(e)
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(O);
-  if (D == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject)
-                  : launch_t<128, false>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject);
-  return causal ? launch_t<64, true>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject)
-                : launch_t<64, false>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject);
+  return launch_prefill<false>(Q, K, V, O, LSE, B, H, S, D, scale, causal, stream, wait_limit_ns,
+                               inject);
+}
+
+cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int S, int D, float scale, int causal,
+                               cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
+  return launch_prefill<true>(Q, K, V, O, LSE, B, H, S, D, scale, causal, stream, wait_limit_ns,
+                              inject);
 }
 
 cudaError_t take_prefill_bf16_error(unsigned int* word) {

@@ -202,12 +202,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 x bf16 -> f32.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   bit 15 A major (0 = K), bit 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation:
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always have the same type), bit 15 A major (0 = K),
+//   bit 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// bf16 x bf16 -> f32
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_f32acc(M, N, b_mn_major, false);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -476,6 +482,19 @@ __device__ __forceinline__ float add_bf16_hi(uint32_t w, float acc) {
       : "=f"(d) : "r"(w), "f"(acc));
   return d;
 }
+// the same for a packed f16 pair
+__device__ __forceinline__ float add_f16_lo(uint32_t w, float acc) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}"
+      : "=f"(d) : "r"(w), "f"(acc));
+  return d;
+}
+__device__ __forceinline__ float add_f16_hi(uint32_t w, float acc) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
+      : "=f"(d) : "r"(w), "f"(acc));
+  return d;
+}
 
 // 2^x for a pair, on the FMA pipe: x = n + f with n = round(x) (the 1.5*2^23
 // shifter leaves n in the low mantissa bits), 2^f from the degree-3 minimax
@@ -501,6 +520,12 @@ __device__ __forceinline__ float2 exp2_poly2(float2 x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// two floats -> packed f16x2, `lo` in the low half (round to nearest even)
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

@@ -69,6 +69,17 @@ int mha_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
             int B, int H, int S, int D, float scale, int causal, void* stream);
 
 /*
+ * The same operation on IEEE half precision (f16) inputs and outputs: the
+ * page's own kernel is written for half-precision data ("Hand-written masked
+ * multi-head attention CUDA kernel", section 3.3).  Arguments and results as
+ * mha_fwd, with Q, K, V, O f16 [B, H, S, D].  The probabilities are rounded
+ * to f16 before the product with V (both operands of one tensor-core product
+ * have the same type); accumulation is fp32.
+ */
+int mha_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                int B, int H, int S, int D, float scale, int causal, void* stream);
+
+/*
  * The same operation with float32 inputs and outputs, computed in fp32 on
  * the CUDA cores (no reduced-precision tensor-core arithmetic anywhere).
  * Arguments as mha_fwd, with Q, K, V, O float [B, H, S, D].  D : 64 or 128.
@@ -99,6 +110,13 @@ int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float*
  */
 int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
                void* O, int B, int H, int D, float scale, void* stream);
+
+/*
+ * mha_decode on f16 data: q, Kcache, Vcache and O are f16 with the layouts
+ * above; everything else (seqlens, scratch, asynchrony, errors) as mha_decode.
+ */
+int mha_decode_f16(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
+                   void* O, int B, int H, int D, float scale, void* stream);
 
 /*
  * mha_decode without allocating anything.  This entry point has no

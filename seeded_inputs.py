@@ -2,15 +2,16 @@
 
 This module draws random numbers and stores them; it holds none of the
 attention arithmetic.  Both sides get the same values: the CUDA path takes
-the raw bf16 bit patterns (or float32 values), the oracle takes the float32
-values that those bit patterns represent exactly.
+the raw 16-bit patterns (bf16 or f16; float32 values for the fp32 path), the
+oracle takes the float32 values that those bit patterns represent exactly.
 
 Recipe (no public dataset or benchmark suite is involved anywhere; every
 tensor is i.i.d. Gaussian from a fixed seed):
   * one numpy PCG64 stream per tensor, seeded with the pair (seed, stream id),
     stream ids 0 = Q/q, 1 = K, 2 = V, 3 = sequence lengths;
   * float32 standard normals times the requested standard deviation;
-  * for bf16 tensors, round-to-nearest-even to bf16 (ties to even mantissa);
+  * for bf16 or f16 tensors, round-to-nearest-even to that type (ties to even
+    mantissa);
   * decode sequence lengths uniform on the integers [len_lo, len_hi].
 """
 from __future__ import annotations
@@ -46,11 +47,22 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to IEEE half (nearest, ties to even); returns uint16 bit patterns."""
+    with np.errstate(over="ignore"):  # beyond 65504 rounds to infinity, as IEEE says
+        return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """The float32 value each f16 bit pattern represents (exact)."""
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
 @dataclass
 class Tensor:
-    """One input tensor: float32 values and, for bf16 tensors, their bit patterns."""
+    """One input tensor: float32 values and, for 16-bit tensors, their bit patterns."""
     values: np.ndarray          # float32, exactly the value the kernel sees
-    bits: np.ndarray | None     # uint16 bf16 patterns, or None for an fp32 tensor
+    bits: np.ndarray | None     # uint16 bf16 or f16 patterns, or None for an fp32 tensor
 
     @property
     def shape(self):
@@ -61,10 +73,13 @@ def make_tensor(seed: int, stream: int, shape, std: float, dtype: str) -> Tensor
     x = normal_f32(seed, stream, shape, std)
     if dtype == "f32":
         return Tensor(x, None)
-    if dtype != "bf16":
-        raise ValueError(dtype)
-    bits = bf16_bits(x)
-    return Tensor(bf16_to_f32(bits), bits)
+    if dtype == "bf16":
+        bits = bf16_bits(x)
+        return Tensor(bf16_to_f32(bits), bits)
+    if dtype == "f16":
+        bits = f16_bits(x)
+        return Tensor(f16_to_f32(bits), bits)
+    raise ValueError(dtype)
 
 
 @dataclass
@@ -104,8 +119,9 @@ class DecodeInputs:
 
 
 def decode_inputs(B: int, H: int, D: int, seed: int, len_lo: int = 512, len_hi: int = 8192,
-                  seqlens=None, std: float = 1.0, scale: float | None = None) -> DecodeInputs:
-    """One bf16 query per (sequence, head) and a packed ragged bf16 cache.
+                  seqlens=None, std: float = 1.0, scale: float | None = None,
+                  dtype: str = "bf16") -> DecodeInputs:
+    """One query per (sequence, head) and a packed ragged cache (bf16 or f16).
 
     The cache holds the sequences back to back: token t of sequence b, head h
     is row (sum_{b'<b} L_b' + t) * H + h of a [sum L, H, D] array.
@@ -115,13 +131,14 @@ def decode_inputs(B: int, H: int, D: int, seed: int, len_lo: int = 512, len_hi: 
     seqlens = np.ascontiguousarray(seqlens, dtype=np.int32)
     total = int(seqlens.sum())
     return DecodeInputs(
-        make_tensor(seed, STREAM_Q, (B, H, D), std, "bf16"),
-        make_tensor(seed, STREAM_K, (total, H, D), std, "bf16"),
-        make_tensor(seed, STREAM_V, (total, H, D), std, "bf16"),
+        make_tensor(seed, STREAM_Q, (B, H, D), std, dtype),
+        make_tensor(seed, STREAM_K, (total, H, D), std, dtype),
+        make_tensor(seed, STREAM_V, (total, H, D), std, dtype),
         seqlens, B, H, D, (1.0 / math.sqrt(D)) if scale is None else float(scale))
 
 
-# The five synthetic workloads: shapes, distributions and seeds.
+# The five synthetic workloads (shapes, distributions and seeds), then the
+# same bench shapes on f16 data.
 WORKLOADS = {
     "prefill_f32_b1h2s128d64": dict(kind="prefill", B=1, H=2, S=128, D=64, dtype="f32",
                                     qk_std=1.0, seed=1001, causal=(True,)),
@@ -133,6 +150,10 @@ WORKLOADS = {
                                                 len_lo=512, len_hi=8192),
     "prefill_bf16_b2h16s16384d64": dict(kind="prefill", B=2, H=16, S=16384, D=64, dtype="bf16",
                                         qk_std=1.0, seed=1005, causal=(True,)),
+    "prefill_f16_b4h32s4096d128_qk3": dict(kind="prefill", B=4, H=32, S=4096, D=128, dtype="f16",
+                                           qk_std=3.0, seed=1006, causal=(True, False)),
+    "decode_f16_b16h32d128_len512_8192": dict(kind="decode", B=16, H=32, D=128, seed=1007,
+                                               len_lo=512, len_hi=8192, dtype="f16"),
 }
 
 
@@ -141,4 +162,5 @@ def workload_inputs(name: str):
     if w["kind"] == "prefill":
         return prefill_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], qk_std=w["qk_std"],
                               dtype=w["dtype"])
-    return decode_inputs(w["B"], w["H"], w["D"], w["seed"], w["len_lo"], w["len_hi"])
+    return decode_inputs(w["B"], w["H"], w["D"], w["seed"], w["len_lo"], w["len_hi"],
+                         dtype=w.get("dtype", "bf16"))

@@ -15,9 +15,9 @@ TOL_LSE = 1e-3
 
 
 def dev_tensor(t, dtype, device="cuda"):
-    """seeded_inputs.Tensor -> torch tensor on the device (bf16 from its bit patterns)."""
-    if dtype == torch.bfloat16:
-        return torch.from_numpy(t.bits.view(np.int16)).view(torch.bfloat16).to(device)
+    """seeded_inputs.Tensor -> torch tensor on the device (bf16 / f16 from its bit patterns)."""
+    if dtype in (torch.bfloat16, torch.float16):
+        return torch.from_numpy(t.bits.view(np.int16)).view(dtype).to(device)
     return torch.from_numpy(np.ascontiguousarray(t.values)).to(device)
 
 
