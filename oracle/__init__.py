@@ -53,6 +53,10 @@ def _declare(lib):
     lib.oracle_attention_rows.argtypes = [
         f32p, f32p, f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_double, ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, ctypes.c_int, intp]
+    lib.oracle_attention_rows_kl.restype = ctypes.c_int
+    lib.oracle_attention_rows_kl.argtypes = [
+        f32p, f32p, f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_double, ctypes.c_int, i32p, i64p, ctypes.c_int64, f64p, f64p, ctypes.c_int, intp]
     lib.oracle_decode.restype = ctypes.c_int
     lib.oracle_decode.argtypes = [
         f32p, f32p, f32p, i32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -85,12 +89,15 @@ class OracleResult(tuple):
     threads: int
 
 
-def attention(Q, K, V, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None):
+def attention(Q, K, V, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None,
+              key_lens=None):
     """Prefill attention in fp64.
 
     Q, K, V: float arrays [B, H, S, D] (bf16 inputs are passed as the float32
     values they represent exactly).  ``rows``: optional flat row ids
-    (b*H + h)*S + i.  Returns (O, LSE): O [B,H,S,D] and LSE [B,H,S] in float64
+    (b*H + h)*S + i.  ``key_lens``: optional int [B], each in [0, S]: only keys
+    j < key_lens[b] of sequence b exist (a row without a valid key gets O = 0,
+    LSE = -inf).  Returns (O, LSE): O [B,H,S,D] and LSE [B,H,S] in float64
     when ``rows`` is None, else O [len(rows), D] and LSE [len(rows)].
     """
     lib = lib or load_library()
@@ -109,8 +116,14 @@ def attention(Q, K, V, scale: float, causal: bool, rows=None, nthreads: int = 0,
     O = np.empty((n, D), dtype=np.float64)
     LSE = np.empty((n,), dtype=np.float64)
     used = ctypes.c_int(0)
-    rc = lib.oracle_attention_rows(
-        qp, kp, vp, B, H, S, D, float(scale), int(bool(causal)), rp, n,
+    if key_lens is not None:
+        kl = np.ascontiguousarray(key_lens, dtype=np.int32)
+        assert kl.shape == (B,)
+        klp = kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    else:
+        klp = None
+    rc = lib.oracle_attention_rows_kl(
+        qp, kp, vp, B, H, S, D, float(scale), int(bool(causal)), klp, rp, n,
         O.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
         LSE.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nthreads), ctypes.byref(used))
     if rc != 0:

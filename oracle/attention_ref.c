@@ -26,6 +26,11 @@
  * the natural log of the softmax denominator, written as m + ln(Z) with m the
  * row maximum.
  *
+ * Key padding (optional): with per-sequence key lengths L_b, key j of
+ * sequence b exists only when j < L_b, the padded scores being -inf (page
+ * "Week 4 CUDA notes" section 2.2 sets padded positions to -inf before the
+ * softmax).  A row with no valid key has O = 0 and LSE = -inf.
+ *
  * Everything is evaluated in double: float inputs are widened exactly, every
  * product and sum is double, nothing is rounded back.  No blocking, fusion or
  * reordering: each row is one pass over its valid keys to get the scores,
@@ -41,12 +46,17 @@
 
 /* One output row of prefill attention.
  * q: D doubles-worth of query (float), K,V: S x D rows of one (b,h) slice.
- * n_valid: number of keys the row may see (i+1 when causal, S otherwise).
+ * n_valid: number of keys the row may see (keys 0..n_valid-1).
  * s: scratch of at least n_valid doubles. */
 static void attention_row(const float *q, const float *K, const float *V,
                           int64_t n_valid, int64_t D, double scale,
                           double *s, double *o, double *lse)
 {
+    if (n_valid == 0) { /* no valid key: empty sum */
+        for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
     /* scores s_j = scale * sum_d q_d k_jd  (page 3, section 2: QK^T/sqrt(d_k)) */
     for (int64_t j = 0; j < n_valid; ++j) {
         double dot = 0.0;
@@ -84,6 +94,7 @@ typedef struct {
     double *O, *LSE;
     int tid, nthreads;
     int status;
+    const int32_t *key_lens; /* [B] key lengths, or NULL: every sequence has S keys */
 } prefill_job;
 
 static void *prefill_worker(void *arg)
@@ -99,6 +110,10 @@ static void *prefill_worker(void *arg)
         const float *base_k = jb->K + bh * jb->S * jb->D;
         const float *base_v = jb->V + bh * jb->S * jb->D;
         int64_t n_valid = jb->causal ? i + 1 : jb->S; /* keys j <= i (page 3, 2.2) */
+        if (jb->key_lens) { /* and j < L_b: both bounds keep a prefix of the keys */
+            int64_t L = jb->key_lens[bh / jb->H];
+            if (n_valid > L) n_valid = L;
+        }
         attention_row(base_q, base_k, base_v, n_valid, jb->D, jb->scale, s,
                       jb->O + r * jb->D, jb->LSE + r);
     }
@@ -115,18 +130,22 @@ static int resolve_threads(int nthreads)
 
 /*
  * Prefill oracle.  Q, K, V: float32 [B, H, S, D] contiguous.
+ * key_lens: int32 [B], each in [0, S], or NULL (every sequence has S keys).
  * rows == NULL: every row, O is [B*H*S, D], LSE is [B*H*S].
  * rows != NULL: nrows flat row ids (b*H + h)*S + i; O is [nrows, D] and LSE
  * [nrows], in the order given.  Returns 0 on success, the number of threads
  * actually used is written to *threads_used when it is not NULL.
  */
-int oracle_attention_rows(const float *Q, const float *K, const float *V,
-                          int64_t B, int64_t H, int64_t S, int64_t D,
-                          double scale, int causal,
-                          const int64_t *rows, int64_t nrows,
-                          double *O, double *LSE, int nthreads, int *threads_used)
+int oracle_attention_rows_kl(const float *Q, const float *K, const float *V,
+                             int64_t B, int64_t H, int64_t S, int64_t D,
+                             double scale, int causal, const int32_t *key_lens,
+                             const int64_t *rows, int64_t nrows,
+                             double *O, double *LSE, int nthreads, int *threads_used)
 {
     if (B < 0 || H < 0 || S < 0 || D < 1) return 2;
+    if (key_lens)
+        for (int64_t b = 0; b < B; ++b)
+            if (key_lens[b] < 0 || key_lens[b] > S) return 2;
     if (!rows) nrows = B * H * S;
     if (rows)
         for (int64_t r = 0; r < nrows; ++r)
@@ -138,7 +157,7 @@ int oracle_attention_rows(const float *Q, const float *K, const float *V,
     pthread_t *th = (pthread_t *)calloc((size_t)nt, sizeof(pthread_t));
     if (!jobs || !th) { free(jobs); free(th); return 1; }
     for (int t = 0; t < nt; ++t) {
-        prefill_job j = {Q, K, V, B, H, S, D, scale, causal, rows, nrows, O, LSE, t, nt, 0};
+        prefill_job j = {Q, K, V, B, H, S, D, scale, causal, rows, nrows, O, LSE, t, nt, 0, key_lens};
         jobs[t] = j;
     }
     for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, prefill_worker, &jobs[t]);
@@ -151,6 +170,17 @@ int oracle_attention_rows(const float *Q, const float *K, const float *V,
     free(jobs);
     free(th);
     return status;
+}
+
+/* The same without key padding. */
+int oracle_attention_rows(const float *Q, const float *K, const float *V,
+                          int64_t B, int64_t H, int64_t S, int64_t D,
+                          double scale, int causal,
+                          const int64_t *rows, int64_t nrows,
+                          double *O, double *LSE, int nthreads, int *threads_used)
+{
+    return oracle_attention_rows_kl(Q, K, V, B, H, S, D, scale, causal, NULL, rows, nrows,
+                                    O, LSE, nthreads, threads_used);
 }
 
 /*

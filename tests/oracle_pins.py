@@ -36,8 +36,10 @@ def _small_grid(rng, shape, denom=8, lo=-12, hi=12):
     return (rng.integers(lo, hi + 1, size=shape) / denom).astype(np.float32)
 
 
-def _decimal_attention(Q, K, V, scale, causal):
-    """Brute force: full masked score matrix, exp without max shift, 50 digits."""
+def _decimal_attention(Q, K, V, scale, causal, key_lens=None):
+    """Brute force: full masked score matrix, exp without max shift, 50 digits.
+    With ``key_lens`` keys j >= key_lens[b] are masked too; a row with no valid
+    key gets O = 0 and LSE = -inf (the empty sum)."""
     ctx = decimal.Context(prec=50)
     Dm = lambda x: ctx.create_decimal_from_float(float(x))
     B, H, S, D = Q.shape
@@ -49,13 +51,17 @@ def _decimal_attention(Q, K, V, scale, causal):
             for i in range(S):
                 w = []
                 for j in range(S):
-                    if causal and j > i:
+                    if (causal and j > i) or (key_lens is not None and j >= key_lens[b]):
                         w.append(ctx.create_decimal(0))  # exp(-inf)
                         continue
                     dot = sum((Dm(Q[b, h, i, d]) * Dm(K[b, h, j, d]) for d in range(D)),
                               ctx.create_decimal(0))
                     w.append(ctx.exp(ctx.multiply(sc, dot)))
                 Z = sum(w, ctx.create_decimal(0))
+                if Z == 0:
+                    O[b, h, i, :] = 0.0
+                    L[b, h, i] = -math.inf
+                    continue
                 for d in range(D):
                     num = sum((w[j] * Dm(V[b, h, j, d]) for j in range(S)), ctx.create_decimal(0))
                     O[b, h, i, d] = float(ctx.divide(num, Z))
@@ -286,6 +292,81 @@ def check_page_causal_count(lib):
     assert kept == S * (S + 1) // 2
 
 
+def check_key_lens_bruteforce_decimal(lib):
+    """Key padding against the 50-digit brute force, empty sequences included."""
+    rng = np.random.default_rng(17)
+    for causal in (True, False):
+        for (B, H, S, D), kl in (((3, 1, 6, 3), [6, 2, 0]), ((2, 2, 5, 2), [1, 4])):
+            Q = rng.standard_normal((B, H, S, D)).astype(np.float32)
+            K = rng.standard_normal((B, H, S, D)).astype(np.float32)
+            V = rng.standard_normal((B, H, S, D)).astype(np.float32)
+            O, L = oracle.attention(Q, K, V, 0.6, causal, lib=lib, key_lens=kl)
+            Ob, Lb = _decimal_attention(Q, K, V, 0.6, causal, key_lens=kl)
+            assert np.max(np.abs(O - Ob)) <= 1e-13, ("O", causal, kl)
+            fin = np.isfinite(Lb)
+            assert np.array_equal(np.isfinite(L), fin), ("LSE finite", causal, kl)
+            assert np.max(np.abs(L[fin] - Lb[fin])) <= 1e-13, ("LSE", causal, kl)
+            assert np.all(L[~fin] == -np.inf)
+
+
+def check_key_lens_library_softmax(lib):
+    """Key padding against scipy's softmax / logsumexp on the masked scores."""
+    from scipy.special import logsumexp, softmax
+    rng = np.random.default_rng(19)
+    B, H, S, D = 3, 2, 41, 8
+    kl = np.array([41, 17, 1], np.int32)
+    Q = (2 * rng.standard_normal((B, H, S, D))).astype(np.float32)
+    K = (2 * rng.standard_normal((B, H, S, D))).astype(np.float32)
+    V = rng.standard_normal((B, H, S, D)).astype(np.float32)
+    scale = 1 / math.sqrt(D)
+    for causal in (True, False):
+        O, L = oracle.attention(Q, K, V, scale, causal, lib=lib, key_lens=kl)
+        s = scale * np.einsum("bhid,bhjd->bhij", Q.astype(np.float64), K.astype(np.float64))
+        keep = np.arange(S)[None, None, None, :] < kl[:, None, None, None]
+        if causal:
+            keep = keep & np.tril(np.ones((S, S), dtype=bool))[None, None]
+        s = np.where(keep, s, -np.inf)
+        Oref = softmax(s, axis=-1) @ V.astype(np.float64)
+        Lref = logsumexp(s, axis=-1)
+        assert np.max(np.abs(O - Oref)) <= 1e-12, causal
+        assert np.max(np.abs(L - Lref)) <= 1e-12, causal
+
+
+def check_key_lens_zero_query_mean(lib):
+    """Q = 0: every valid key has the same weight, so O_i is the mean of the
+    first n values and LSE_i = ln n, n = min(i + 1, L_b) (causal) or L_b."""
+    rng = np.random.default_rng(23)
+    B, H, S, D = 3, 2, 13, 4
+    kl = np.array([13, 5, 1], np.int32)
+    Q = np.zeros((B, H, S, D), np.float32)
+    K = rng.standard_normal((B, H, S, D)).astype(np.float32)
+    V = rng.standard_normal((B, H, S, D)).astype(np.float32)
+    Vd = V.astype(np.float64)
+    for causal in (True, False):
+        O, L = oracle.attention(Q, K, V, 0.5, causal, lib=lib, key_lens=kl)
+        for b in range(B):
+            for i in range(S):
+                n = min(i + 1, int(kl[b])) if causal else int(kl[b])
+                assert np.max(np.abs(O[b, :, i] - Vd[b, :, :n].mean(axis=1))) <= 1e-14
+                assert np.max(np.abs(L[b, :, i] - math.log(n))) <= 1e-14
+
+
+def check_padding_keys_do_not_matter(lib):
+    """Keys at or past L_b are padding: replacing their K and V rows by other
+    numbers changes nothing, bit for bit."""
+    rng = np.random.default_rng(29)
+    B, H, S, D = 2, 3, 23, 6
+    kl = np.array([9, 23], np.int32)
+    Q, K, V = (rng.standard_normal((B, H, S, D)).astype(np.float32) for _ in range(3))
+    K2, V2 = K.copy(), V.copy()
+    K2[0, :, 9:] = 50 * rng.standard_normal((H, S - 9, D))
+    V2[0, :, 9:] = 1e3
+    for causal in (True, False):
+        O, L = oracle.attention(Q, K, V, 0.4, causal, lib=lib, key_lens=kl)
+        O2, L2 = oracle.attention(Q, K2, V2, 0.4, causal, lib=lib, key_lens=kl)
+        assert np.array_equal(O, O2) and np.array_equal(L, L2), causal
+
+
 ALL_CHECKS = [
     check_bruteforce_decimal,
     check_library_softmax,
@@ -300,4 +381,8 @@ ALL_CHECKS = [
     check_rows_subset,
     check_decode_is_last_causal_row,
     check_page_causal_count,
+    check_key_lens_bruteforce_decimal,
+    check_key_lens_library_softmax,
+    check_key_lens_zero_query_mean,
+    check_padding_keys_do_not_matter,
 ]

@@ -24,6 +24,9 @@ MUTANTS = {
     "no_normalisation": ("double a = s[j] / Z;", "double a = s[j];"),
     "lse_without_max": ("*lse = m + log(Z);", "*lse = log(Z);"),
     "max_not_subtracted_from_lse": ("*lse = m + log(Z);", "*lse = m * 0.5 + log(Z);"),
+    "key_lens_ignored": ("int64_t L = jb->key_lens[bh / jb->H];", "int64_t L = jb->S;"),
+    "key_lens_indexed_by_head": ("int64_t L = jb->key_lens[bh / jb->H];",
+                                 "int64_t L = jb->key_lens[bh % jb->B];"),
     "decode_ignores_sequence_offset": ("jb->Kc + ((jb->offs[b] + t) * H + h) * D",
                                        "jb->Kc + ((t) * H + h) * D"),
     "decode_value_offset": ("jb->Vc + ((jb->offs[b] + t) * H + h) * D",
