@@ -45,6 +45,10 @@ def _declare(lib):
     lib.mha_fwd.restype = i
     lib.mha_fwd_f16.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.mha_fwd_f16.restype = i
+    lib.mha_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.mha_fwd_varlen.restype = i
+    lib.mha_fwd_varlen_f16.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.mha_fwd_varlen_f16.restype = i
     lib.mha_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.mha_fwd_f32.restype = i
     lib.mha_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
@@ -105,7 +109,7 @@ def _check(t: torch.Tensor, name: str, dtype, shape, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _prefill(entry, dtype, Q, K, V, O, LSE, scale, causal, stream, want_lse):
+def _prefill(entry, dtype, Q, K, V, O, LSE, scale, causal, stream, want_lse, key_lens=None):
     if Q.dim() != 4:
         raise ValueError("Q must be [B, H, S, D]")
     B, H, S, D = Q.shape
@@ -121,9 +125,12 @@ def _prefill(entry, dtype, Q, K, V, O, LSE, scale, causal, stream, want_lse):
         _check(LSE, "LSE", torch.float32, (B, H, S), dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    st = getattr(_load(), entry)(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
-                                 LSE.data_ptr() if LSE is not None else None,
-                                 B, H, S, D, float(scale), int(bool(causal)),
+    ptrs = [Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+            LSE.data_ptr() if LSE is not None else None]
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, (B,), dev)
+        ptrs.append(key_lens.data_ptr())
+    st = getattr(_load(), entry)(*ptrs, B, H, S, D, float(scale), int(bool(causal)),
                                  _stream_ptr(stream, dev))
     if st != MHA_OK:
         raise MHAError(st, entry)
@@ -139,6 +146,21 @@ def mha_fwd_f16(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None,
     """f16 [B,H,S,D] prefill; returns (O, LSE).  See include/mha.h: mha_fwd_f16."""
     return _prefill("mha_fwd_f16", torch.float16, Q, K, V, O, LSE, scale, causal, stream,
                     want_lse)
+
+
+def mha_fwd_varlen(Q, K, V, key_lens, O=None, LSE=None, scale=None, causal=True, stream=None,
+                   want_lse=True):
+    """bf16 prefill with key padding: key_lens int32 [B] on the device (keys
+    j >= key_lens[b] are excluded).  See include/mha.h: mha_fwd_varlen."""
+    return _prefill("mha_fwd_varlen", torch.bfloat16, Q, K, V, O, LSE, scale, causal, stream,
+                    want_lse, key_lens=key_lens)
+
+
+def mha_fwd_varlen_f16(Q, K, V, key_lens, O=None, LSE=None, scale=None, causal=True, stream=None,
+                       want_lse=True):
+    """f16 prefill with key padding.  See include/mha.h: mha_fwd_varlen_f16."""
+    return _prefill("mha_fwd_varlen_f16", torch.float16, Q, K, V, O, LSE, scale, causal, stream,
+                    want_lse, key_lens=key_lens)
 
 
 def mha_fwd_f32(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, want_lse=True):

@@ -10,14 +10,17 @@ namespace mha {
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
+// key_lens: device int32 [B] of valid key counts (key padding), or nullptr.
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                                int B, int H, int S, int D, float scale, int causal,
-                                cudaStream_t stream, uint64_t wait_limit_ns, int inject);
+                                const int* key_lens, int B, int H, int S, int D, float scale,
+                                int causal, cudaStream_t stream, uint64_t wait_limit_ns,
+                                int inject);
 
 // The same on f16 inputs and outputs (P rounded to f16).
 cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                               int B, int H, int S, int D, float scale, int causal,
-                               cudaStream_t stream, uint64_t wait_limit_ns, int inject);
+                               const int* key_lens, int B, int H, int S, int D, float scale,
+                               int causal, cudaStream_t stream, uint64_t wait_limit_ns,
+                               int inject);
 
 cudaError_t launch_prefill_f32(const float* Q, const float* K, const float* V, float* O,
                                float* LSE, int B, int H, int S, int D, float scale, int causal,

@@ -64,7 +64,7 @@ int mha_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, in
   const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
   if (st != MHA_OK) return st;
   const cudaError_t e =
-      mha::launch_prefill_bf16(Q, K, V, O, LSE, B, H, S, D, scale, causal,
+      mha::launch_prefill_bf16(Q, K, V, O, LSE, nullptr, B, H, S, D, scale, causal,
                                static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
                                g_fault_injection.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
@@ -75,7 +75,35 @@ int mha_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE
   const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
   if (st != MHA_OK) return st;
   const cudaError_t e =
-      mha::launch_prefill_f16(Q, K, V, O, LSE, B, H, S, D, scale, causal,
+      mha::launch_prefill_f16(Q, K, V, O, LSE, nullptr, B, H, S, D, scale, causal,
+                              static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
+                              g_fault_injection.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+int mha_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   const int* key_lens, int B, int H, int S, int D, float scale, int causal,
+                   void* stream) {
+  const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
+  if (st != MHA_OK) return st;
+  if (!key_lens) return MHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(key_lens) & 3u) return MHA_ERR_MISALIGNED;
+  const cudaError_t e =
+      mha::launch_prefill_bf16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal,
+                               static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
+                               g_fault_injection.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+int mha_fwd_varlen_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       const int* key_lens, int B, int H, int S, int D, float scale, int causal,
+                       void* stream) {
+  const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
+  if (st != MHA_OK) return st;
+  if (!key_lens) return MHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(key_lens) & 3u) return MHA_ERR_MISALIGNED;
+  const cudaError_t e =
+      mha::launch_prefill_f16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal,
                               static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
                               g_fault_injection.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);

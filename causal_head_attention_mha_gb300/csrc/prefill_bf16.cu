@@ -144,15 +144,17 @@ struct RingWalk {
   }
 };
 
-// Key-tile counts of one item (query block qp of 256 rows).
+// Key-tile counts of one item (query block qp of 256 rows) whose sequence
+// has L valid keys (L = S without key padding; keys j >= L are padding).
 struct ItemShape {
-  int nA, nB, nkv;  // key tiles used by tile A, by tile B (0: B lies past S), loaded
-  __device__ ItemShape(int qp, int S, bool causal) {
-    const int n_kt = (S + BN - 1) / BN;
-    const bool hasB = (qp * 2 + 1) * BM < S;
+  int nA, nB, nkv;  // key tiles used by tile A, by tile B, loaded
+  bool hasB;        // tile B has query rows (it does not lie past S)
+  __device__ ItemShape(int qp, int S, int L, bool causal) {
+    const int n_kt = (L + BN - 1) / BN;
+    hasB = (qp * 2 + 1) * BM < S;
     if (causal) {
-      nA = 2 * qp + 1;
-      nB = hasB ? 2 * qp + 2 : 0;
+      nA = min(2 * qp + 1, n_kt);
+      nB = hasB ? min(2 * qp + 2, n_kt) : 0;
     } else {
       nA = n_kt;
       nB = hasB ? n_kt : 0;
@@ -247,9 +249,15 @@ template <int D, bool CAUSAL, bool F16>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                              const CUtensorMap& tmV, uint16_t* __restrict__ O,
                                              float* __restrict__ lse, int S, int BH, float c_log2,
+                                             const int* __restrict__ key_lens, int H,
                                              uint64_t wait_limit_ns, int inject) {
   using C = Cfg<D>;
   using E = Elem<F16>;
+  // valid keys of the sequence of (b, h) = bh: key_lens[b] clamped to [0, S],
+  // or S without key padding
+  auto key_len = [&](int bh) {
+    return key_lens == nullptr ? S : min(max(__ldg(key_lens + bh / H), 0), S);
+  };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -321,7 +329,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       int nq[2] = {0, 0};  // Q_X copies issued
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
-        const ItemShape sh(qp, S, CAUSAL);
+        const ItemShape sh(qp, S, key_len(bh), CAUSAL);
         for (int x = 0; ok && x < 2; ++x) {
           if ((x ? sh.nB : sh.nA) == 0) continue;
           if (nq[x] >= 1)
@@ -347,7 +355,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       int bh, qp, n = 0;
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
-        const ItemShape sh(qp, S, CAUSAL);
+        const ItemShape sh(qp, S, key_len(bh), CAUSAL);
         // units in order: K_0 V_0 K_1 V_1 ... (paired: one unit per key tile)
         const int nunits = (C::PAIRED ? 1 : 2) * sh.nkv;
         for (int u = 0; ok && u < nunits; ++u, ++n) {
@@ -438,7 +446,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
         umma_commit(bar(C::B_SFULL + x));
       };
       while (ok && sch.next(bh, qp)) {
-        const ItemShape sh(qp, S, CAUSAL);
+        const ItemShape sh(qp, S, key_len(bh), CAUSAL);
         const int nx[2] = {sh.nA, sh.nB};
         for (int x = 0; ok && x < 2; ++x)
           if (nx[x] > 0) ok = mbar_wait(bar(C::B_QFULL + x), bit(2 + x), wc, SITE_MMA_Q);
@@ -533,7 +541,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       bool ok = true;
       const uint32_t pfull_a = bar(C::B_PFULL);
       while (ok && sch.next(bh, qp)) {
-        const ItemShape sh(qp, S, CAUSAL);
+        const ItemShape sh(qp, S, key_len(bh), CAUSAL);
         for (int j = 0; ok && j <= sh.nkv; ++j) {
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
           ring.step(pv_step, s_step);
@@ -568,10 +576,21 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
     bool failed = false;
     while (!failed && sch.next(bh, qp)) {
-      const ItemShape sh(qp, S, CAUSAL);
+      const int L = key_len(bh);
+      const ItemShape sh(qp, S, L, CAUSAL);
       const int nx = x ? sh.nB : sh.nA;
-      if (nx == 0) continue;
       const int q = (2 * qp + x) * BM + row;
+      if (nx == 0) {
+        // a sequence without any valid key (L = 0): its rows are the empty
+        // sum, O = 0 and LSE = -inf
+        if ((x == 0 || sh.hasB) && q < S) {
+          uint16_t* orow = O + (static_cast<size_t>(bh) * S + q) * D;
+#pragma unroll
+          for (int c = 0; c < D; c += 8) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
+          if (lse != nullptr) lse[static_cast<size_t>(bh) * S + q] = -INFINITY;
+        }
+        continue;
+      }
       float m_run = -INFINITY;  // reference maximum, log2 units
       float l_run = 0.f;        // sum of fp32 weights: gives the log-sum-exp
       float lp_run = 0.f;       // sum of bf16-rounded weights: normalises O
@@ -581,9 +600,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
         tc_fence_after();
         uint32_t s[128];
         tmem_ld_32x32b_x128(tS, s);
-        const bool need_mask = CAUSAL ? (j == nx - 1) : (j * BN + BN > S);
+        const bool need_mask = CAUSAL ? (j == nx - 1) : (j * BN + BN > L);
         // last key index (within this tile) the row may use
-        const int lim = (CAUSAL ? min(q, S - 1) : (S - 1)) - j * BN;
+        const int lim = (CAUSAL ? min(q, L - 1) : (L - 1)) - j * BN;
         auto mask = [&](uint32_t (&v)[128]) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
@@ -745,8 +764,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
                         float* __restrict__ lse, int S, int BH, float c_log2,
-                        uint64_t wait_limit_ns, int inject) {
-  prefill_body<D, CAUSAL, false>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, wait_limit_ns, inject);
+                        const int* __restrict__ key_lens, int H, uint64_t wait_limit_ns,
+                        int inject) {
+  prefill_body<D, CAUSAL, false>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H, wait_limit_ns,
+                                 inject);
 }
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -754,8 +775,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
                        float* __restrict__ lse, int S, int BH, float c_log2,
-                       uint64_t wait_limit_ns, int inject) {
-  prefill_body<D, CAUSAL, true>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, wait_limit_ns, inject);
+                       const int* __restrict__ key_lens, int H, uint64_t wait_limit_ns,
+                       int inject) {
+  prefill_body<D, CAUSAL, true>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H, wait_limit_ns,
+                                inject);
 }
 
 // ---------------------------------------------------------------- host side
@@ -796,8 +819,8 @@ bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D, bool f
 
 template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                     uint16_t* O, float* lse, int BH, int S, float c_log2,
-                     cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
+                     uint16_t* O, float* lse, int BH, int S, float c_log2, const int* key_lens,
+                     int H, cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
   auto kern = F16 ? prefill_f16_kernel<D, CAUSAL> : prefill_bf16_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -814,14 +837,15 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   const int nsm = device_sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = static_cast<unsigned>(items < nsm ? items : nsm);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, O, lse, S, BH, c_log2, wait_limit_ns, inject);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, O, lse, S, BH, c_log2, key_lens, H,
+                                         wait_limit_ns, inject);
   return cudaGetLastError();
 }
 
 template <bool F16>
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                           int B, int H, int S, int D, float scale, int causal,
-                           cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
+                           const int* key_lens, int B, int H, int S, int D, float scale,
+                           int causal, cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   if (!encode_bhsd(&mq, Q, BH, S, D, F16) || !encode_bhsd(&mk, K, BH, S, D, F16) ||
@@ -829,27 +853,29 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     return cudaErrorInvalidValue;
   const float c_log2 = scale * 1.44269504088896340736f;  // scale * log2(e)
   uint16_t* o = static_cast<uint16_t*>(O);
-  if (D == 128)
-    return causal ? launch_t<128, true, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject)
-                  : launch_t<128, false, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject);
-  return causal ? launch_t<64, true, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject)
-                : launch_t<64, false, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, stream, wait_limit_ns, inject);
+#define MHA_LAUNCH(DD, CC) \
+  launch_t<DD, CC, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, stream, wait_limit_ns, inject)
+  if (D == 128) return causal ? MHA_LAUNCH(128, true) : MHA_LAUNCH(128, false);
+  return causal ? MHA_LAUNCH(64, true) : MHA_LAUNCH(64, false);
+#undef MHA_LAUNCH
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                                int B, int H, int S, int D, float scale, int causal,
-                                cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
-  return launch_prefill<false>(Q, K, V, O, LSE, B, H, S, D, scale, causal, stream, wait_limit_ns,
-                               inject);
+                                const int* key_lens, int B, int H, int S, int D, float scale,
+                                int causal, cudaStream_t stream, uint64_t wait_limit_ns,
+                                int inject) {
+  return launch_prefill<false>(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, stream,
+                               wait_limit_ns, inject);
 }
 
 cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                               int B, int H, int S, int D, float scale, int causal,
-                               cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
-  return launch_prefill<true>(Q, K, V, O, LSE, B, H, S, D, scale, causal, stream, wait_limit_ns,
-                              inject);
+                               const int* key_lens, int B, int H, int S, int D, float scale,
+                               int causal, cudaStream_t stream, uint64_t wait_limit_ns,
+                               int inject) {
+  return launch_prefill<true>(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, stream,
+                              wait_limit_ns, inject);
 }
 
 cudaError_t take_prefill_bf16_error(unsigned int* word) {

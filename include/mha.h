@@ -80,6 +80,29 @@ int mha_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE
                 int B, int H, int S, int D, float scale, int causal, void* stream);
 
 /*
+ * mha_fwd with key padding: sequence b of the batch has key_lens[b] valid
+ * keys, and key j of sequence b takes part in no row when j >= key_lens[b]
+ * (its score is -inf before the softmax, as page "Week 4 CUDA notes" section
+ * 2.2 does for padded positions).  With causal = 1 query i uses key j when
+ * j <= i and j < key_lens[b].  A row with no valid key (key_lens[b] = 0)
+ * gets O = 0 and LSE = -inf.  Key tiles at or past key_lens[b] are neither
+ * loaded nor computed.  Query rows i >= key_lens[b] are computed like any
+ * other row (they are not masked as queries).
+ *
+ *   key_lens : const int32 [B] in DEVICE memory; each value in [0, S] (values
+ *              outside are clamped to that range on the device).
+ *   other arguments as mha_fwd (bf16).
+ */
+int mha_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   const int* key_lens, int B, int H, int S, int D, float scale, int causal,
+                   void* stream);
+
+/* mha_fwd_varlen on f16 data (the types of mha_fwd_f16). */
+int mha_fwd_varlen_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       const int* key_lens, int B, int H, int S, int D, float scale,
+                       int causal, void* stream);
+
+/*
  * The same operation with float32 inputs and outputs, computed in fp32 on
  * the CUDA cores (no reduced-precision tensor-core arithmetic anywhere).
  * Arguments as mha_fwd, with Q, K, V, O float [B, H, S, D].  D : 64 or 128.
