@@ -113,6 +113,22 @@ def prefill_flops(B, H, S, D, causal=True):
     return (2.0 if causal else 4.0) * B * H * S * S * D
 
 
+def valid_keys(x, rows, causal=True):
+    """Keys each flat row (b*H + h)*S + i attends to: min(i + 1, L_b) causal,
+    L_b otherwise (L_b = S without key padding)."""
+    rows = np.asarray(rows)
+    i = rows % x.S
+    L = x.key_lens[rows // (x.H * x.S)] if x.key_lens is not None else x.S
+    return np.minimum(i + 1, L) if causal else np.broadcast_to(L, rows.shape)
+
+
+def prefill_flops_varlen(H, S, D, key_lens, causal=True):
+    """Useful flops (two products, 2 flops per multiply-add) with key padding."""
+    L = np.asarray(key_lens, np.float64)
+    per_seq = L * (L + 1) / 2 + (S - L) * L if causal else S * L
+    return 4.0 * H * D * float(np.sum(per_seq))
+
+
 def decode_bytes(B, H, D, seqlens):
     return 2.0 * float(np.sum(seqlens)) * H * D * 2 + 2.0 * B * H * D * 2
 
@@ -176,10 +192,10 @@ def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None, worklo
 
     def run(n):
         rows = np.sort(rng.choice(total_rows, size=n, replace=False))
-        i = rows % x.S
-        flops = float(np.sum(4.0 * (i + 1) * x.D)) if causal else 4.0 * x.S * x.D * n
+        flops = float(np.sum(4.0 * valid_keys(x, rows, causal) * x.D))
         t0 = time.perf_counter()
-        res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows)
+        res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows,
+                               key_lens=x.key_lens)
         return time.perf_counter() - t0, flops, res.threads
 
     dt, _, _ = run(2048)
@@ -204,10 +220,10 @@ def run_reference(args, rank, world):
 
     def step(n):
         rows = np.sort(rng.choice(total_rows, size=n, replace=False))
-        i = rows % x.S
         t0 = time.perf_counter()
-        res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, True, rows=rows)
-        return time.perf_counter() - t0, float(np.sum(4.0 * (i + 1) * x.D)), res.threads
+        res = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, True, rows=rows,
+                               key_lens=x.key_lens)
+        return time.perf_counter() - t0, float(np.sum(4.0 * valid_keys(x, rows) * x.D)), res.threads
 
     dt, _, _ = step(32)
     n = int(max(16, min(100000, budget_per_step / max(dt / 32, 1e-6))))
@@ -259,7 +275,11 @@ def run_ours(args, rank, world, dist):
     wp = si.WORKLOADS[args.prefill_workload]
     wd = si.WORKLOADS[args.decode_workload]
     pdt, ddt = wp["dtype"], wd.get("dtype", "bf16")
-    fwd = mha.mha_fwd_f16 if pdt == "f16" else mha.mha_fwd
+    varlen = "key_len_lo" in wp
+    if varlen:
+        fwd = mha.mha_fwd_varlen_f16 if pdt == "f16" else mha.mha_fwd_varlen
+    else:
+        fwd = mha.mha_fwd_f16 if pdt == "f16" else mha.mha_fwd
     dec = mha.mha_decode_f16 if ddt == "f16" else mha.mha_decode
     # each rank works on its own batch (weak scaling, no collective on the data path)
     if do_prefill:
@@ -268,7 +288,13 @@ def run_ours(args, rank, world, dist):
         Q, K, V = dev16(xp.Q, pdt), dev16(xp.K, pdt), dev16(xp.V, pdt)
         O = torch.empty_like(Q)
         LSE = torch.empty((xp.B, xp.H, xp.S), dtype=torch.float32, device=dev)
-        flops = prefill_flops(xp.B, xp.H, xp.S, xp.D, True)
+        if varlen:
+            xp.key_lens = si.prefill_key_lens(xp.B, rank_seed(wp["seed"], rank), wp["key_len_lo"],
+                                              wp["key_len_hi"])
+            KL = torch.from_numpy(xp.key_lens).to(dev)
+            flops = prefill_flops_varlen(xp.H, xp.S, xp.D, xp.key_lens, True)
+        else:
+            flops = prefill_flops(xp.B, xp.H, xp.S, xp.D, True)
     if do_decode:
         xd = si.decode_inputs(wd["B"], wd["H"], wd["D"], rank_seed(wd["seed"], rank), wd["len_lo"],
                               wd["len_hi"], dtype=ddt)
@@ -279,7 +305,10 @@ def run_ours(args, rank, world, dist):
         nsplit = mha.mha_decode_num_splits(xd.B, xd.H)
 
     def prefill():
-        fwd(Q, K, V, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
+        if varlen:
+            fwd(Q, K, V, KL, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
+        else:
+            fwd(Q, K, V, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
 
     def decode():
         dec(q, Kc, Vc, sl, O=Od, scale=xd.scale, stream=stream)
@@ -395,6 +424,9 @@ def run_ours(args, rank, world, dist):
         line.update({"value": value, "unit": "TFLOP/s"})
         cfg.update({"prefill": {"B": xp.B, "H": xp.H, "S": xp.S, "D": xp.D, "causal": True,
                                 "qk_std": wp["qk_std"], "flops_per_step": flops}})
+        if varlen:
+            # flops count each row's valid keys: min(i + 1, L_b)
+            cfg["prefill"]["key_lens"] = [int(v) for v in xp.key_lens]
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                     "traffic": traffic_for("prefill_" + pdt, args.prefill_workload),

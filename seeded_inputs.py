@@ -93,6 +93,12 @@ class PrefillInputs:
     D: int
     scale: float
     dtype: str
+    key_lens: np.ndarray | None = None  # int32 [B] valid keys per sequence (key padding)
+
+
+def prefill_key_lens(B: int, seed: int, lo: int, hi: int) -> np.ndarray:
+    """Per-sequence key lengths, uniform on the integers [lo, hi]."""
+    return np.ascontiguousarray(_rng(seed, STREAM_LEN).integers(lo, hi + 1, size=B), np.int32)
 
 
 def prefill_inputs(B: int, H: int, S: int, D: int, seed: int, qk_std: float = 1.0,
@@ -154,13 +160,21 @@ WORKLOADS = {
                                            qk_std=3.0, seed=1006, causal=(True, False)),
     "decode_f16_b16h32d128_len512_8192": dict(kind="decode", B=16, H=32, D=128, seed=1007,
                                                len_lo=512, len_hi=8192, dtype="f16"),
+    # key padding: the bench shape with per-sequence key lengths U{1024..4096}
+    "prefill_varlen_bf16_b4h32s4096d128": dict(kind="prefill", B=4, H=32, S=4096, D=128,
+                                               dtype="bf16", qk_std=1.0, seed=1008,
+                                               causal=(True, False), key_len_lo=1024,
+                                               key_len_hi=4096),
 }
 
 
 def workload_inputs(name: str):
     w = WORKLOADS[name]
     if w["kind"] == "prefill":
-        return prefill_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], qk_std=w["qk_std"],
-                              dtype=w["dtype"])
+        x = prefill_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], qk_std=w["qk_std"],
+                           dtype=w["dtype"])
+        if "key_len_lo" in w:
+            x.key_lens = prefill_key_lens(w["B"], w["seed"], w["key_len_lo"], w["key_len_hi"])
+        return x
     return decode_inputs(w["B"], w["H"], w["D"], w["seed"], w["len_lo"], w["len_hi"],
                          dtype=w.get("dtype", "bf16"))

@@ -132,3 +132,18 @@ def test_varlen_rejects_missing_lengths():
     with pytest.raises(ValueError):
         mha().mha_fwd_varlen(dev_tensor(x.Q, t), dev_tensor(x.K, t), dev_tensor(x.V, t),
                              torch.zeros(2, dtype=torch.int32, device="cuda"))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_workload_sampled(causal):
+    """The full-size key-padding workload the benchmark can time, on sampled rows."""
+    from gpu_util import sample_rows
+    x = si.workload_inputs("prefill_varlen_bf16_b4h32s4096d128")
+    O, L = _run(x, x.key_lens, causal, "bf16")
+    rows = sample_rows(x.B, x.H, x.S, n_bh=12, rows_per_bh=96, seed=9)
+    Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows,
+                              key_lens=x.key_lens)
+    Og = O.view(-1, x.D)[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    Lg = L.view(-1)[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_bf16_close(Og, Or, Lg, Lr, what=f"varlen workload causal={causal}")
+    assert torch.isfinite(O.float()).all()
