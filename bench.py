@@ -46,14 +46,22 @@ TRAFFIC = {
     # profiles/prefill_bf16_d128_causal_b4h32s4096.md
     "prefill": {"kernel": "prefill_bf16", "workload": PREFILL_WORKLOAD,
                 "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "137e9c8533c1bda16384bee0f29909909bca976f0ea31d6d4a6af384eaa87a39", "bytes_per_launch": 520408064},
+                "sha256": "fcf9f504ad4ba218c16dbc5f495c9f0ad287dd0143f71a61d5e1a2eb070f692d", "bytes_per_launch": 521596928},
     # profiles/prefill_bf16_d64_causal_b2h16s16384.md
     "prefill_d64": {"kernel": "prefill_bf16", "workload": "prefill_bf16_b2h16s16384d64",
                     "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "137e9c8533c1bda16384bee0f29909909bca976f0ea31d6d4a6af384eaa87a39", "bytes_per_launch": 251825664},
+                    "sha256": "fcf9f504ad4ba218c16dbc5f495c9f0ad287dd0143f71a61d5e1a2eb070f692d", "bytes_per_launch": 252577792},
+    # profiles/prefill_f16_d128_causal_b4h32s4096.md
+    "prefill_f16": {"kernel": "prefill_f16", "workload": "prefill_f16_b4h32s4096d128_qk3",
+                    "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                    "sha256": "fcf9f504ad4ba218c16dbc5f495c9f0ad287dd0143f71a61d5e1a2eb070f692d", "bytes_per_launch": 526535168},
     # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
     "decode": {"kernel": "decode", "workload": DECODE_WORKLOAD, "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
-               "sha256": "cd2f0b5822aba3d400a9c178d01b3d3db17d173476f07ce74399531d28ca7f9c", "bytes_per_launch": 1201866048},
+               "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1201886720},
+    # profiles/decode_split_f16_d128_b16h32_len512_8192.md
+    "decode_f16": {"kernel": "decode", "workload": "decode_f16_b16h32d128_len512_8192",
+                   "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
+                   "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1292623616},
 }
 
 
@@ -432,7 +440,7 @@ def run_ours(args, rank, world, dist):
                     "traffic": traffic_for("prefill_" + pdt, args.prefill_workload),
                     "peak_source": f"bf16_tflops (burst), of {peak_src}",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "kernel": f"prefill_{pdt}_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
+                    "kernel": f"prefill_{pdt}{'_varlen' if varlen else ''}_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
         line["roofline"] = roofline
     if do_decode:
         gbs = whole_job_rate(world, K_ * dbytes, td) / 1e9

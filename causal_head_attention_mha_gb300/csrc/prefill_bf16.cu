@@ -245,7 +245,7 @@ struct Elem<true> {  // f16
   static __device__ __forceinline__ float add_hi(uint32_t w, float a) { return add_f16_hi(w, a); }
 };
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, bool VARLEN>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                              const CUtensorMap& tmV, uint16_t* __restrict__ O,
                                              float* __restrict__ lse, int S, int BH, float c_log2,
@@ -253,10 +253,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
                                              uint64_t wait_limit_ns, int inject) {
   using C = Cfg<D>;
   using E = Elem<F16>;
-  // valid keys of the sequence of (b, h) = bh: key_lens[b] clamped to [0, S],
-  // or S without key padding
+  // valid keys of the sequence of (b, h) = bh: key_lens[b] clamped to [0, S]
+  // with key padding (VARLEN), else S
   auto key_len = [&](int bh) {
-    return key_lens == nullptr ? S : min(max(__ldg(key_lens + bh / H), 0), S);
+    if constexpr (VARLEN) return min(max(__ldg(key_lens + bh / H), 0), S);
+    (void)bh;
+    return S;
   };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -583,7 +585,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       if (nx == 0) {
         // a sequence without any valid key (L = 0): its rows are the empty
         // sum, O = 0 and LSE = -inf
-        if ((x == 0 || sh.hasB) && q < S) {
+        if (VARLEN && (x == 0 || sh.hasB) && q < S) {
           uint16_t* orow = O + (static_cast<size_t>(bh) * S + q) * D;
 #pragma unroll
           for (int c = 0; c < D; c += 8) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
@@ -757,29 +759,23 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
   }
 }
 
-// The kernels: one per 16-bit input type, the same body.
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
-                        const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
-                        float* __restrict__ lse, int S, int BH, float c_log2,
-                        const int* __restrict__ key_lens, int H, uint64_t wait_limit_ns,
-                        int inject) {
-  prefill_body<D, CAUSAL, false>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H, wait_limit_ns,
-                                 inject);
-}
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_f16_kernel(const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,
-                       float* __restrict__ lse, int S, int BH, float c_log2,
-                       const int* __restrict__ key_lens, int H, uint64_t wait_limit_ns,
-                       int inject) {
-  prefill_body<D, CAUSAL, true>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H, wait_limit_ns,
-                                inject);
-}
+// The kernels: one per 16-bit input type, with and without key padding, the
+// same body.
+#define MHA_PREFILL_KERNEL(NAME, F16, VARLEN)                                              \
+  template <int D, bool CAUSAL>                                                             \
+  __global__ void __launch_bounds__(kThreads, 1)                                            \
+      NAME(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, \
+           const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,                \
+           float* __restrict__ lse, int S, int BH, float c_log2,                             \
+           const int* __restrict__ key_lens, int H, uint64_t wait_limit_ns, int inject) {    \
+    prefill_body<D, CAUSAL, F16, VARLEN>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H,  \
+                                         wait_limit_ns, inject);                            \
+  }
+MHA_PREFILL_KERNEL(prefill_bf16_kernel, false, false)
+MHA_PREFILL_KERNEL(prefill_f16_kernel, true, false)
+MHA_PREFILL_KERNEL(prefill_bf16_varlen_kernel, false, true)
+MHA_PREFILL_KERNEL(prefill_f16_varlen_kernel, true, true)
+#undef MHA_PREFILL_KERNEL
 
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -817,12 +813,13 @@ bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D, bool f
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, bool VARLEN>
 cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                      uint16_t* O, float* lse, int BH, int S, float c_log2, const int* key_lens,
                      int H, cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
-  auto kern = F16 ? prefill_f16_kernel<D, CAUSAL> : prefill_bf16_kernel<D, CAUSAL>;
+  auto kern = VARLEN ? (F16 ? prefill_f16_varlen_kernel<D, CAUSAL> : prefill_bf16_varlen_kernel<D, CAUSAL>)
+                     : (F16 ? prefill_f16_kernel<D, CAUSAL> : prefill_bf16_kernel<D, CAUSAL>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // The softmax warpgroups raise their register limit with registers the
@@ -853,10 +850,14 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     return cudaErrorInvalidValue;
   const float c_log2 = scale * 1.44269504088896340736f;  // scale * log2(e)
   uint16_t* o = static_cast<uint16_t*>(O);
-#define MHA_LAUNCH(DD, CC) \
-  launch_t<DD, CC, F16>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, stream, wait_limit_ns, inject)
-  if (D == 128) return causal ? MHA_LAUNCH(128, true) : MHA_LAUNCH(128, false);
-  return causal ? MHA_LAUNCH(64, true) : MHA_LAUNCH(64, false);
+#define MHA_LAUNCH(DD, CC, VL) \
+  launch_t<DD, CC, F16, VL>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, stream, wait_limit_ns, inject)
+  if (key_lens != nullptr) {
+    if (D == 128) return causal ? MHA_LAUNCH(128, true, true) : MHA_LAUNCH(128, false, true);
+    return causal ? MHA_LAUNCH(64, true, true) : MHA_LAUNCH(64, false, true);
+  }
+  if (D == 128) return causal ? MHA_LAUNCH(128, true, false) : MHA_LAUNCH(128, false, false);
+  return causal ? MHA_LAUNCH(64, true, false) : MHA_LAUNCH(64, false, false);
 #undef MHA_LAUNCH
 }
 
