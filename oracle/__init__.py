@@ -9,7 +9,9 @@ pthreads across rows); this module compiles it with gcc and marshals numpy
 arrays to it.  What it computes is the definition on the page "Hand-written
 masked multi-head attention CUDA kernel: underlying logic and practice",
 section 2 (A = softmax(QK^T/sqrt(d_k) + M), O = A V with M = -inf above the
-diagonal), with the valid-key rule j <= i of its section 2.2.
+diagonal), with the valid-key rule j <= i of its section 2.2.  The fused
+Q, K, V projection (``qkv_projection``) is one fp64 numpy matrix product and
+a reshape, the definition of section 2 (Q = X W_Q, ...).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force at high precision, closed forms, invariants, a library softmax)
@@ -162,3 +164,27 @@ def decode(q, Kc, Vc, seqlens, scale: float, nthreads: int = 0, lib=None):
     res = OracleResult((O, LSE))
     res.threads = used.value
     return res
+
+
+def qkv_projection(X, W, H: int, D: int):
+    """The fused Q, K, V projection in fp64 (test infrastructure, like the rest
+    of this module).
+
+    Page "Hand-written masked multi-head attention CUDA kernel" section 2:
+    Q = X W_Q, K = X W_K, V = X W_V, with (section 2.1) X of shape (batch,
+    seq_len, hidden) and each W of shape (hidden, heads * head_dim); page
+    "Week 4 CUDA notes" section 2.1 fuses the three products into one GEMM,
+    so W here is [W_Q | W_K | W_V], shape (hidden, 3 * H * D).
+
+    X: float [B, S, hidden]; W: float [hidden, 3*H*D] (16-bit inputs are passed
+    as the float32 values they represent exactly).  Returns (Q, K, V), each
+    float64 [B, H, S, D]: column n = c*H*D + h*D + d of X W is head h, feature
+    d of Q (c = 0), K (c = 1) or V (c = 2).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    B, S, hidden = X.shape
+    assert W.shape == (hidden, 3 * H * D)
+    Y = np.matmul(X.reshape(B * S, hidden), W)          # one product, fp64
+    Y = Y.reshape(B, S, 3, H, D).transpose(2, 0, 3, 1, 4)  # [3, B, H, S, D]
+    return Y[0].copy(), Y[1].copy(), Y[2].copy()

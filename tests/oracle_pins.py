@@ -367,6 +367,53 @@ def check_padding_keys_do_not_matter(lib):
         assert np.array_equal(O, O2) and np.array_equal(L, L2), causal
 
 
+def check_qkv_bruteforce_fsum(lib):
+    """The fused projection against an exactly rounded sum (math.fsum of the
+    exact double products of float32 values) on a tiny case."""
+    rng = np.random.default_rng(31)
+    B, S, hid, H, D = 2, 3, 5, 2, 2
+    X = rng.standard_normal((B, S, hid)).astype(np.float32)
+    W = rng.standard_normal((hid, 3 * H * D)).astype(np.float32)
+    Q, K, V = oracle.qkv_projection(X, W, H, D)
+    out = (Q, K, V)
+    for b in range(B):
+        for s_ in range(S):
+            for c in range(3):
+                for h in range(H):
+                    for d in range(D):
+                        n = c * H * D + h * D + d
+                        ref = math.fsum(float(X[b, s_, k]) * float(W[k, n]) for k in range(hid))
+                        assert abs(out[c][b, h, s_, d] - ref) <= 1e-14 * (1 + abs(ref))
+
+
+def check_qkv_selection_and_layout(lib):
+    """One-hot weights copy chosen input features exactly; one-hot inputs
+    reproduce rows of W, placed at [c][b, h, s, d] with n = c*H*D + h*D + d."""
+    rng = np.random.default_rng(37)
+    B, S, hid, H, D = 2, 4, 6, 3, 2
+    N = 3 * H * D
+    X = rng.standard_normal((B, S, hid)).astype(np.float32)
+    pick = rng.integers(0, hid, size=N)
+    W = np.zeros((hid, N), np.float32)
+    W[pick, np.arange(N)] = 1.0
+    Q, K, V = oracle.qkv_projection(X, W, H, D)
+    for c, T in enumerate((Q, K, V)):
+        for h in range(H):
+            for d in range(D):
+                n = c * H * D + h * D + d
+                assert np.array_equal(T[:, h, :, d], X[:, :, pick[n]].astype(np.float64))
+    W2 = rng.standard_normal((hid, N)).astype(np.float32)
+    X2 = np.zeros((B, S, hid), np.float32)
+    X2[1, 2, 4] = 1.0
+    Q, K, V = oracle.qkv_projection(X2, W2, H, D)
+    row = W2[4].astype(np.float64).reshape(3, H, D)
+    for c, T in enumerate((Q, K, V)):
+        assert np.array_equal(T[1, :, 2, :], row[c])
+        mask = np.ones(T.shape, bool)
+        mask[1, :, 2, :] = False
+        assert np.all(T[mask] == 0.0)
+
+
 ALL_CHECKS = [
     check_bruteforce_decimal,
     check_library_softmax,
@@ -385,4 +432,6 @@ ALL_CHECKS = [
     check_key_lens_library_softmax,
     check_key_lens_zero_query_mean,
     check_padding_keys_do_not_matter,
+    check_qkv_bruteforce_fsum,
+    check_qkv_selection_and_layout,
 ]

@@ -50,3 +50,36 @@ def test_mutant_is_caught(name, tmp_path):
             caught.append(check.__name__)
             break
     assert caught, f"no pin fails for planted mistake {name}"
+
+
+# The fused projection is numpy (no C): its planted mistakes are textual
+# changes to oracle.qkv_projection's source, executed in place of it.
+PY_MUTANTS = {
+    "qkv_q_and_k_swapped": ("return Y[0].copy(), Y[1].copy(), Y[2].copy()",
+                            "return Y[1].copy(), Y[0].copy(), Y[2].copy()"),
+    "qkv_heads_and_features_swapped": ("Y = Y.reshape(B, S, 3, H, D).transpose(2, 0, 3, 1, 4)",
+                                       "Y = Y.reshape(B, S, 3, D, H).transpose(2, 0, 4, 1, 3)"),
+    "qkv_float32_product": ("Y = np.matmul(X.reshape(B * S, hidden), W)",
+                            "Y = np.matmul(X.reshape(B * S, hidden).astype(np.float32), "
+                            "W.astype(np.float32))"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_projection_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import numpy as np
+    old, new = PY_MUTANTS[name]
+    src = inspect.getsource(oracle.qkv_projection)
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    monkeypatch.setattr(oracle, "qkv_projection", ns["qkv_projection"])
+    caught = False
+    for check in (oracle_pins.check_qkv_bruteforce_fsum, oracle_pins.check_qkv_selection_and_layout):
+        try:
+            check(None)
+        except AssertionError:
+            caught = True
+            break
+    assert caught, f"no pin fails for planted mistake {name}"
