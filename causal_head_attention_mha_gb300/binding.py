@@ -57,6 +57,8 @@ def _declare(lib):
     lib.mha_decode_f16.restype = i
     lib.mha_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
     lib.mha_decode_noalloc.restype = i
+    lib.mha_qkv_proj.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.mha_qkv_proj.restype = i
     lib.mha_decode_num_splits.argtypes = [i, i]
     lib.mha_decode_num_splits.restype = i
     lib.mha_get_device_status.argtypes = [vp]
@@ -232,6 +234,30 @@ def mha_decode_noalloc(q, Kcache, Vcache, seqlens, O, scale=None, stream=None):
     if st != MHA_OK:
         raise MHAError(st, "mha_decode_noalloc")
     return O
+
+
+def mha_qkv_proj(X, W, H: int, D: int, Q=None, K=None, V=None, stream=None):
+    """Fused projection [Q | K | V] = X [W_Q | W_K | W_V], bf16; returns (Q, K, V),
+    each [B, H, S, D].  X: [B, S, hidden]; W: [hidden, 3*H*D].  See include/mha.h:
+    mha_qkv_proj."""
+    if X.dim() != 3:
+        raise ValueError("X must be [B, S, hidden]")
+    B, S, hidden = X.shape
+    dev = X.device
+    _check(X, "X", torch.bfloat16, (B, S, hidden), dev)
+    _check(W, "W", torch.bfloat16, (hidden, 3 * H * D), dev)
+    out = []
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t is None:
+            t = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev)
+        _check(t, name, torch.bfloat16, (B, H, S, D), dev)
+        out.append(t)
+    st = _load().mha_qkv_proj(X.data_ptr(), W.data_ptr(), out[0].data_ptr(), out[1].data_ptr(),
+                              out[2].data_ptr(), B, S, hidden, int(H), int(D),
+                              _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, "mha_qkv_proj")
+    return tuple(out)
 
 
 def mha_decode_num_splits(B: int, H: int) -> int:

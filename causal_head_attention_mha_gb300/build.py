@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(OUT_DIR, "libmha.so")
-SOURCES = ["mha_api.cu", "prefill_bf16.cu", "prefill_f32.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["mha_api.cu", "prefill_bf16.cu", "prefill_f32.cu", "decode.cu", "decode_noalloc.cu",
+           "gemm_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

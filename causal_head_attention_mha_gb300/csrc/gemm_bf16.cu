@@ -1,0 +1,352 @@
+// gemm_bf16.cu — the fused Q, K, V projection on the sm_103a tensor cores
+// (tcgen05 + TMEM) fed by TMA, bf16 in and out, fp32 accumulation.
+//
+// Method: page "Hand-written masked multi-head attention CUDA kernel:
+// underlying logic and practice" section 2 (Q = X W_Q, K = X W_K,
+// V = X W_V) with the shapes of its section 2.1 (X: batch x seq_len x
+// hidden; each W: hidden x heads*head_dim).  Page "Week 4 CUDA notes"
+// section 2.1 fuses the three products into one GEMM: W = [W_Q | W_K | W_V]
+// (hidden x 3*H*D), Y = X W, and Y is written straight into Q, K and V in the
+// [B, H, S, D] layout the attention kernels read (column n = c*H*D + h*D + d
+// of Y is feature d of head h of Q, K or V for c = 0, 1, 2).
+//
+// Tiles of 128 rows (M = B*S) x 256 columns (N = 3*H*D); K (= hidden) in
+// steps of 64 through a ring of 4 stages, each the 128 x 64 slice of X
+// (K-major, 16 KB) and the 64 x 256 slice of W (MN-major: four 64-column
+// blocks of 8 KB), both 128-byte swizzled.  A persistent grid walks the
+// tiles in groups of 16 row tiles, all column tiles of a group before the
+// next, so a W slice is reused by the group while it is in L2.  Roles:
+//   warp 0       TMA producer of the ring
+//   warp 1       tensor-memory allocation; one thread issues every MMA
+//                (M = 128, N = 256, K = 16; fp32 accumulator in TMEM)
+//   warps 4..7   epilogue: one output row per thread, TMEM -> bf16 ->
+//                16-byte stores into Q, K, V
+// The accumulator is double-buffered (2 x 256 TMEM columns): the epilogue of
+// one tile overlaps the products of the next.  Every wait is bounded in time
+// (an expired wait sets this unit's error word and the CTA winds down).
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace mha {
+
+__device__ unsigned int g_err_gemm_bf16 = 0;
+
+namespace {
+
+constexpr int GM = 128, GN = 256, GK = 64;
+constexpr int kStages = 4;
+constexpr int kGroupM = 16;                    // row tiles per scheduling group
+constexpr int A_BYTES = GM * GK * 2;           // 16 KB
+constexpr int B_BLOCK = GK * 64 * 2;           // one 64-column block of W: 8 KB
+constexpr int B_BYTES = 4 * B_BLOCK;           // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int BAR_OFF = kStages * STAGE_BYTES;
+// barrier indices
+constexpr int B_FULL = 0;                  // [stage] its tiles landed
+constexpr int B_EMPTY = B_FULL + kStages;  // [stage] its last MMA complete
+constexpr int B_AFULL = B_EMPTY + kStages;  // [buffer] the tile's accumulator is final
+constexpr int B_AFREE = B_AFULL + 2;        // [buffer] the epilogue has read it (128 arrivals)
+constexpr int B_DRAIN = B_AFREE + 2;
+constexpr int NBAR = B_DRAIN + 1;
+constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // barriers + flags, alignment slack
+constexpr int kThreads = 256;
+constexpr int kEpiWarp0 = 4;
+static_assert(NBAR * 8 + 8 <= 256, "barrier area");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+enum : uint32_t { GSITE_PROD_EMPTY = 1, GSITE_MMA_FULL, GSITE_MMA_AFREE, GSITE_EPI_AFULL };
+
+// 4 MMAs D += A B over K = 64, both operands in shared memory: A K-major
+// (128-byte swizzle: the next 16 k are 32 bytes further, +2 in the
+// descriptor's address field), B MN-major (the next 16 k are 16 rows =
+// 2048 bytes further, +128).
+__device__ __forceinline__ void umma_ss_kmajor_mnmajor_x4(uint32_t d_tmem, uint64_t adesc,
+                                                          uint64_t bdesc, uint32_t idesc,
+                                                          uint32_t acc_first) {
+  asm volatile("{\n\t"
+               ".reg .pred pf, pt;\n\t"
+               ".reg .b64 a, b;\n\t"
+               "setp.ne.b32 pf, %4, 0;\n\t"
+               "setp.eq.b32 pt, %4, %4;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+               "add.s64 a, %1, 2;\n\t"
+               "add.s64 b, %2, 128;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 a, %1, 4;\n\t"
+               "add.s64 b, %2, 256;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "add.s64 a, %1, 6;\n\t"
+               "add.s64 b, %2, 384;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "}" ::"r"(d_tmem),
+               "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc_first)
+               : "memory");
+}
+
+// 2-D tiled TMA load of box (x, y) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4_g(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                               uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Tile t of the persistent walk -> (row tile, column tile): groups of
+// kGroupM row tiles, column tiles outer within a group.
+struct TileMap {
+  int tiles_m, tiles_n;
+  __device__ void get(int t, int& mt, int& nt) const {
+    const int per_group = kGroupM * tiles_n;
+    const int g = t / per_group, r = t % per_group;
+    const int first = g * kGroupM;
+    const int rows = min(kGroupM, tiles_m - first);
+    mt = first + r % rows;
+    nt = r / rows;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
+                    int M, int N, int Kd, int S, int H, int D, uint64_t wait_limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) -> uint32_t { return sbase + BAR_OFF + 8u * i; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_AFULL + b), 1);
+      mbar_init(bar(B_AFREE + b), 128);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{wait_limit_ns, &g_err_gemm_bf16, abort_flag};
+  const TileMap tmap{(M + GM - 1) / GM, (N + GN - 1) / GN};
+  const int ntiles = tmap.tiles_m * tmap.tiles_n;
+  const int nk = (Kd + GK - 1) / GK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmX);
+      prefetch_tensormap(&tmW);
+      int n = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        int mt, nt;
+        tmap.get(t, mt, nt);
+        for (int kb = 0; kb < nk; ++kb, ++n) {
+          const int st = n % kStages;
+          if (n >= kStages &&
+              !mbar_wait(bar(B_EMPTY + st), ((n / kStages) & 1) ^ 1, wc, GSITE_PROD_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + st * STAGE_BYTES;
+          const uint32_t full = bar(B_FULL + st);
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          // X viewed as [M][Kd]: rows mt*128.., columns kb*64..
+          tma_load_2d(dst, &tmX, full, kb * GK, mt * GM);
+          // W viewed as [Kd][N]: four 64-column blocks of rows kb*64..
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(dst + A_BYTES + j * B_BLOCK, &tmW, full, nt * GN + j * 64, kb * GK);
+        }
+      }
+      if (*abort_flag) {
+        // let every copy still in flight land before the CTA can exit
+        for (int st = 0; st < kStages && st < n; ++st) {
+          const int last = st + ((n - 1 - st) / kStages) * kStages;
+          mbar_wait_drain(bar(B_FULL + st), (last / kStages) & 1, kDrainLimitNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(GM, GN, true);
+      const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
+      auto desc = [&](uint32_t lo) { return (static_cast<uint64_t>(desc_hi) << 32) | lo; };
+      // A: K-major, LBO unused; B: MN-major, LBO = the next 64-column block
+      const uint32_t a_lo0 = (sbase >> 4) | (1u << 16);
+      const uint32_t b_lo0 = ((sbase + A_BYTES) >> 4) | ((B_BLOCK >> 4) << 16);
+      int n = 0, tc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++tc) {
+        const int buf = tc & 1;
+        // the epilogue has read this buffer's previous tile
+        if (tc >= 2 && !mbar_wait(bar(B_AFREE + buf), ((tc >> 1) - 1) & 1, wc, GSITE_MMA_AFREE)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dtm = tmem + static_cast<uint32_t>(buf) * GN;
+        for (int kb = 0; kb < nk; ++kb, ++n) {
+          const int st = n % kStages;
+          if (!mbar_wait(bar(B_FULL + st), (n / kStages) & 1, wc, GSITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t off = static_cast<uint32_t>(st * STAGE_BYTES) >> 4;
+          umma_ss_kmajor_mnmajor_x4(dtm, desc(a_lo0 + off), desc(b_lo0 + off), idesc,
+                                    kb > 0 ? 1u : 0u);
+          umma_commit(bar(B_EMPTY + st));  // the stage is free once these MMAs complete
+        }
+        if (!ok) break;
+        umma_commit(bar(B_AFULL + buf));
+      }
+      // every MMA issued completes before tensor memory is freed
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // row of the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int HD = H * D;
+    bool failed = false;
+    int tc = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
+      const int buf = tc & 1;
+      failed = !__all_sync(0xffffffffu, mbar_wait(bar(B_AFULL + buf), (tc >> 1) & 1, wc, GSITE_EPI_AFULL));
+      if (failed) break;
+      tc_fence_after();
+      int mt, nt;
+      tmap.get(t, mt, nt);
+      const int m = mt * GM + r;
+      const int b = m / S, s = m - (m / S) * S;
+#pragma unroll 1
+      for (int c = 0; c < GN / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(buf) * GN + c * 32, o);
+        const int n0 = nt * GN + c * 32;
+        // N = 3*H*D is a multiple of 32 and D of 32: a 32-column chunk lies in
+        // one head of one of Q, K, V, or entirely past N
+        if (m < M && n0 < N) {
+          const int which = n0 / HD, rem = n0 - which * HD;
+          const int h = rem / D, d0 = rem - h * D;
+          uint16_t* base = which == 0 ? Qo : (which == 1 ? Ko : Vo);
+          uint16_t* dst = base + ((static_cast<size_t>(b) * H + h) * S + s) * D + d0;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            st_global_v4_g(dst + c4 * 8, w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+        }
+      }
+      // the buffer may take the next tile's products
+      tc_fence_before();
+      mbar_arrive(bar(B_AFREE + buf));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// A row-major bf16 matrix [rows][cols] as a 2-D tensor (cols innermost),
+// 128-byte swizzle, box = box_cols x box_rows; reads past the edges give 0.
+bool encode_2d(CUtensorMap* map, const void* ptr, long long rows, long long cols, int box_cols,
+               int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B, int S,
+                            int hidden, int H, int D, cudaStream_t stream,
+                            uint64_t wait_limit_ns) {
+  const int M = B * S, N = 3 * H * D, Kd = hidden;
+  CUtensorMap mx, mw;
+  if (!encode_2d(&mx, X, M, Kd, GK, GM) || !encode_2d(&mw, W, Kd, N, 64, GK))
+    return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(qkv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>((M + GM - 1) / GM) * ((N + GN - 1) / GN);
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = static_cast<unsigned>(tiles < nsm ? tiles : nsm);
+  qkv_proj_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(
+      mx, mw, static_cast<uint16_t*>(Q), static_cast<uint16_t*>(K), static_cast<uint16_t*>(V), M, N,
+      Kd, S, H, D, wait_limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t take_gemm_bf16_error(unsigned int* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_err_gemm_bf16, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_err_gemm_bf16, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mha

@@ -35,8 +35,15 @@ cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, const i
                           void* O, float* ws, int B, int H, int D, int nsplit, float scale,
                           cudaStream_t stream, bool f16);
 
-// Reads and clears the device error word of the prefill translation unit.
+// Fused Q, K, V projection: [Q | K | V] = X [W_Q | W_K | W_V], bf16; X [B*S][hidden],
+// W [hidden][3*H*D] row-major; Q, K, V written as [B, H, S, D].
+cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B, int S,
+                            int hidden, int H, int D, cudaStream_t stream,
+                            uint64_t wait_limit_ns);
+
+// Read and clear the device error word of the prefill / projection translation unit.
 cudaError_t take_prefill_bf16_error(unsigned int* word);
+cudaError_t take_gemm_bf16_error(unsigned int* word);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();

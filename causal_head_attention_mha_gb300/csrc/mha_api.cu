@@ -166,6 +166,23 @@ int mha_decode_f16(const void* q, const void* Kcache, const void* Vcache, const 
   return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, true);
 }
 
+int mha_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B, int S,
+                 int hidden, int H, int D, void* stream) {
+  if (!X || !W || !Q || !K || !V) return MHA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || hidden < 1 || H < 1 || D < 1) return MHA_ERR_INVALID_ARG;
+  const long long M = static_cast<long long>(B) * S, N = 3LL * H * D;
+  if (M * hidden >= (1LL << 31) || N * hidden >= (1LL << 31) || M * N >= (1LL << 31))
+    return MHA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return MHA_ERR_UNSUPPORTED;
+  if (hidden % 8 != 0) return MHA_ERR_UNSUPPORTED;  // rows of X must be 16-byte multiples
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Q) || !aligned16(K) || !aligned16(V))
+    return MHA_ERR_MISALIGNED;
+  const cudaError_t e = mha::launch_qkv_proj(X, W, Q, K, V, B, S, hidden, H, D,
+                                             static_cast<cudaStream_t>(stream),
+                                             g_wait_limit_ns.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
 int mha_decode_num_splits(int B, int H) {
   if (B < 1 || H < 1) return 0;
   const int nsm = mha::device_sm_count();
@@ -176,10 +193,12 @@ int mha_decode_num_splits(int B, int H) {
 int mha_get_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
-  unsigned int word = 0;
+  unsigned int word = 0, word2 = 0;
   e = mha::take_prefill_bf16_error(&word);
   if (e != cudaSuccess) return cuda_fail(e);
-  return word ? MHA_ERR_TIMEOUT : MHA_OK;
+  e = mha::take_gemm_bf16_error(&word2);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return (word | word2) ? MHA_ERR_TIMEOUT : MHA_OK;
 }
 
 const char* mha_status_string(int status) {

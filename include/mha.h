@@ -180,6 +180,23 @@ int mha_decode_noalloc(const void* q, const void* Kcache, const void* Vcache,
 int mha_decode_num_splits(int B, int H);
 
 /*
+ * Fused Q, K, V projection feeding the attention calls: page 3 section 2
+ * (Q = X W_Q, K = X W_K, V = X W_V) with its section 2.1 shapes, the three
+ * products fused into one GEMM as page 1 section 2.1 ("Week 4 CUDA notes")
+ * does.  bf16 in and out, fp32 accumulation on the tensor cores.
+ *
+ *   X       : const bf16 [B, S, hidden] (row-major [B*S][hidden]).
+ *   W       : const bf16 [hidden, 3*H*D] = [W_Q | W_K | W_V] (row-major).
+ *   Q, K, V : bf16 [B, H, S, D], written: Q[b][h][s][d] = sum_k X[b][s][k] *
+ *             W[k][h*D + d]; K uses columns H*D + h*D + d, V 2*H*D + h*D + d.
+ *             This is the layout mha_fwd reads.
+ *   hidden  : >= 1 and a multiple of 8.   D : 64 or 128.
+ *   B*S*hidden, hidden*3*H*D and B*S*3*H*D each < 2^31.
+ */
+int mha_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B, int S,
+                 int hidden, int H, int D, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * bounded waits set.  Returns MHA_OK, MHA_ERR_TIMEOUT when a wait in some
  * kernel of this library ran out since the last call, or MHA_ERR_CUDA when

@@ -143,6 +143,25 @@ def decode_inputs(B: int, H: int, D: int, seed: int, len_lo: int = 512, len_hi: 
         seqlens, B, H, D, (1.0 / math.sqrt(D)) if scale is None else float(scale))
 
 
+@dataclass
+class ProjectionInputs:
+    X: Tensor   # [B, S, hidden]
+    W: Tensor   # [hidden, 3*H*D] = [W_Q | W_K | W_V]
+    B: int
+    S: int
+    hidden: int
+    H: int
+    D: int
+
+
+def projection_inputs(B: int, S: int, hidden: int, H: int, D: int, seed: int) -> ProjectionInputs:
+    """X ~ N(0, 1) and W ~ N(0, 1/hidden) (outputs of order one), bf16."""
+    return ProjectionInputs(
+        make_tensor(seed, STREAM_Q, (B, S, hidden), 1.0, "bf16"),
+        make_tensor(seed, STREAM_K, (hidden, 3 * H * D), 1.0 / math.sqrt(hidden), "bf16"),
+        B, S, hidden, H, D)
+
+
 # The five synthetic workloads (shapes, distributions and seeds), then the
 # same bench shapes on f16 data.
 WORKLOADS = {
@@ -160,6 +179,10 @@ WORKLOADS = {
                                            qk_std=3.0, seed=1006, causal=(True, False)),
     "decode_f16_b16h32d128_len512_8192": dict(kind="decode", B=16, H=32, D=128, seed=1007,
                                                len_lo=512, len_hi=8192, dtype="f16"),
+    # the fused Q/K/V projection feeding the bench's attention shape (LLaMA-7B
+    # layer: hidden 4096 = 32 heads x 128)
+    "qkv_bf16_b4s4096hid4096_h32d128": dict(kind="projection", B=4, S=4096, hidden=4096, H=32,
+                                            D=128, seed=1009),
     # key padding: the bench shape with per-sequence key lengths U{1024..4096}
     "prefill_varlen_bf16_b4h32s4096d128": dict(kind="prefill", B=4, H=32, S=4096, D=128,
                                                dtype="bf16", qk_std=1.0, seed=1008,
@@ -170,6 +193,8 @@ WORKLOADS = {
 
 def workload_inputs(name: str):
     w = WORKLOADS[name]
+    if w["kind"] == "projection":
+        return projection_inputs(w["B"], w["S"], w["hidden"], w["H"], w["D"], w["seed"])
     if w["kind"] == "prefill":
         x = prefill_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], qk_std=w["qk_std"],
                            dtype=w["dtype"])

@@ -99,3 +99,49 @@ def test_status_strings_and_wait_limit(lib):
     assert old == 2_000_000_000
     assert lib.mha_set_wait_limit_ns(0) == 12345
     assert lib.mha_set_wait_limit_ns(0) == 2_000_000_000
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(Q=None), INVALID), (dict(B=0), INVALID), (dict(D=96), UNSUPPORTED),
+    (dict(K=FAKE + 8), MISALIGNED), (dict(scale=0.0), INVALID),
+])
+def test_f16_and_varlen_prefill_validation(lib, kw, expected):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, LSE=None, B=1, H=2, S=128, D=64, scale=0.125,
+             causal=1)
+    a.update(kw)
+    args = (a["Q"], a["K"], a["V"], a["O"], a["LSE"])
+    rest = (a["B"], a["H"], a["S"], a["D"], a["scale"], a["causal"], None)
+    assert lib.mha_fwd_f16(*args, *rest) == expected
+    assert lib.mha_fwd_varlen(*args, FAKE, *rest) == expected
+    assert lib.mha_fwd_varlen_f16(*args, FAKE, *rest) == expected
+
+
+def test_varlen_needs_aligned_lengths(lib):
+    args = (FAKE, FAKE, FAKE, FAKE, None)
+    rest = (1, 2, 128, 64, 0.125, 1, None)
+    assert lib.mha_fwd_varlen(*args, None, *rest) == INVALID
+    assert lib.mha_fwd_varlen(*args, FAKE + 2, *rest) == MISALIGNED
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(q=None), INVALID), (dict(D=32), UNSUPPORTED), (dict(Vc=FAKE + 8), MISALIGNED),
+])
+def test_f16_decode_validation(lib, kw, expected):
+    a = dict(q=FAKE, Kc=FAKE, Vc=FAKE, seqlens=FAKE, O=FAKE, B=2, H=2, D=128, scale=0.1)
+    a.update(kw)
+    assert lib.mha_decode_f16(a["q"], a["Kc"], a["Vc"], a["seqlens"], a["O"], a["B"], a["H"],
+                              a["D"], a["scale"], None) == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(X=None), INVALID), (dict(V=None), INVALID), (dict(B=0), INVALID),
+    (dict(hidden=0), INVALID), (dict(H=0), INVALID),
+    (dict(B=1 << 12, S=1 << 12, hidden=4096), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(hidden=12), UNSUPPORTED),
+    (dict(W=FAKE + 8), MISALIGNED), (dict(Q=FAKE + 4), MISALIGNED),
+])
+def test_qkv_proj_validation(lib, kw, expected):
+    a = dict(X=FAKE, W=FAKE, Q=FAKE, K=FAKE, V=FAKE, B=1, S=128, hidden=256, H=2, D=64)
+    a.update(kw)
+    assert lib.mha_qkv_proj(a["X"], a["W"], a["Q"], a["K"], a["V"], a["B"], a["S"], a["hidden"],
+                            a["H"], a["D"], None) == expected
