@@ -11,7 +11,8 @@ masked multi-head attention CUDA kernel: underlying logic and practice",
 section 2 (A = softmax(QK^T/sqrt(d_k) + M), O = A V with M = -inf above the
 diagonal), with the valid-key rule j <= i of its section 2.2.  The fused
 Q, K, V projection (``qkv_projection``) is one fp64 numpy matrix product and
-a reshape, the definition of section 2 (Q = X W_Q, ...).
+a reshape, the definition of section 2 (Q = X W_Q, ...); the output
+projection (``out_projection``) is the same over the concatenated heads.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force at high precision, closed forms, invariants, a library softmax)
@@ -188,3 +189,21 @@ def qkv_projection(X, W, H: int, D: int):
     Y = np.matmul(X.reshape(B * S, hidden), W)          # one product, fp64
     Y = Y.reshape(B, S, 3, H, D).transpose(2, 0, 3, 1, 4)  # [3, B, H, S, D]
     return Y[0].copy(), Y[1].copy(), Y[2].copy()
+
+
+def out_projection(O, W):
+    """The output projection in fp64 (test infrastructure).
+
+    Page "Week 4 CUDA notes" section 2.1 lists it after attention as one more
+    GEMM: the heads of O are concatenated (feature h*D + d of a row is head h,
+    feature d) and multiplied by W_O, Y = concat_h(O_h) W_O; the same sum per
+    head, Y = sum_h O_h W_O[h*D:(h+1)*D], is the grouped form.
+
+    O: float [B, H, S, D]; W: float [H*D, N].  Returns Y, float64 [B, S, N].
+    """
+    O = np.asarray(O, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    B, H, S, D = O.shape
+    assert W.shape[0] == H * D
+    A = O.transpose(0, 2, 1, 3).reshape(B * S, H * D)   # rows (b, s), columns h*D + d
+    return np.matmul(A, W).reshape(B, S, W.shape[1])

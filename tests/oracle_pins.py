@@ -414,6 +414,36 @@ def check_qkv_selection_and_layout(lib):
         assert np.all(T[mask] == 0.0)
 
 
+def check_out_proj_bruteforce_fsum(lib):
+    """The output projection against exactly rounded sums on a tiny case."""
+    rng = np.random.default_rng(41)
+    B, H, S, D, N = 2, 3, 4, 2, 5
+    O = rng.standard_normal((B, H, S, D)).astype(np.float32)
+    W = rng.standard_normal((H * D, N)).astype(np.float32)
+    Y = oracle.out_projection(O, W)
+    for b in range(B):
+        for s_ in range(S):
+            for n in range(N):
+                ref = math.fsum(float(O[b, h, s_, d]) * float(W[h * D + d, n])
+                                for h in range(H) for d in range(D))
+                assert abs(Y[b, s_, n] - ref) <= 1e-14 * (1 + abs(ref))
+
+
+def check_out_proj_head_order(lib):
+    """A single 1 at O[b, h, s, d] makes row (b, s) of Y row h*D + d of W_O
+    and every other row zero: the heads are concatenated head-major."""
+    rng = np.random.default_rng(43)
+    B, H, S, D, N = 2, 3, 5, 4, 6
+    W = rng.standard_normal((H * D, N)).astype(np.float32)
+    for (b, h, s_, d) in ((1, 2, 3, 1), (0, 0, 0, 3), (1, 1, 4, 0)):
+        O = np.zeros((B, H, S, D), np.float32)
+        O[b, h, s_, d] = 1.0
+        Y = oracle.out_projection(O, W)
+        assert np.array_equal(Y[b, s_], W[h * D + d].astype(np.float64))
+        Y[b, s_] = 0.0
+        assert not np.any(Y)
+
+
 ALL_CHECKS = [
     check_bruteforce_decimal,
     check_library_softmax,
@@ -434,4 +464,6 @@ ALL_CHECKS = [
     check_padding_keys_do_not_matter,
     check_qkv_bruteforce_fsum,
     check_qkv_selection_and_layout,
+    check_out_proj_bruteforce_fsum,
+    check_out_proj_head_order,
 ]

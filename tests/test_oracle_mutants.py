@@ -65,6 +65,35 @@ PY_MUTANTS = {
 }
 
 
+OUT_MUTANTS = {
+    "out_proj_features_head_minor": ("A = O.transpose(0, 2, 1, 3).reshape(B * S, H * D)",
+                                     "A = O.transpose(0, 2, 3, 1).reshape(B * S, H * D)"),
+    "out_proj_float32_product": ("return np.matmul(A, W).reshape(B, S, W.shape[1])",
+                                 "return np.matmul(A.astype(np.float32), W.astype(np.float32))"
+                                 ".reshape(B, S, W.shape[1])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(OUT_MUTANTS))
+def test_out_projection_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import numpy as np
+    old, new = OUT_MUTANTS[name]
+    src = inspect.getsource(oracle.out_projection)
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    monkeypatch.setattr(oracle, "out_projection", ns["out_projection"])
+    caught = False
+    for check in (oracle_pins.check_out_proj_bruteforce_fsum, oracle_pins.check_out_proj_head_order):
+        try:
+            check(None)
+        except AssertionError:
+            caught = True
+            break
+    assert caught, f"no pin fails for planted mistake {name}"
+
+
 @pytest.mark.parametrize("name", sorted(PY_MUTANTS))
 def test_projection_mutant_is_caught(name, monkeypatch):
     import inspect
