@@ -467,13 +467,116 @@ def run_ours(args, rank, world, dist):
     return 0
 
 
+QKV_WORKLOAD = "qkv_bf16_b4s4096hid4096_h32d128"
+OUTPROJ_WORKLOAD = "outproj_bf16_b4h32s4096d128_n4096"
+
+
+def run_projections(args, rank, world, dist):
+    """--only projections: the two GEMMs around attention (mha_qkv_proj, then
+    mha_out_proj) on the bench's layer shape, device-resident inputs, each
+    kernel timed with CUDA events on the launching stream; `value` is their
+    combined TFLOP/s (2 * M * K * N flops per GEMM).  Not part of the default step."""
+    import torch
+    import causal_head_attention_mha_gb300 as mha
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mha.load_library()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    def dev16(t):
+        return torch.from_numpy(t.bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    wq, wo = si.WORKLOADS[QKV_WORKLOAD], si.WORKLOADS[OUTPROJ_WORKLOAD]
+    xq = si.projection_inputs(wq["B"], wq["S"], wq["hidden"], wq["H"], wq["D"],
+                              rank_seed(wq["seed"], rank))
+    xo = si.out_projection_inputs(wo["B"], wo["H"], wo["S"], wo["D"], wo["n_out"],
+                                  rank_seed(wo["seed"], rank))
+    X, Wqkv = dev16(xq.X), dev16(xq.W)
+    shp = (xq.B, xq.H, xq.S, xq.D)
+    Q, K, V = (torch.empty(shp, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    O, Wo = dev16(xo.O), dev16(xo.W)
+    Y = torch.empty((xo.B, xo.S, xo.n_out), dtype=torch.bfloat16, device=dev)
+    M = xq.B * xq.S
+    f_qkv = 2.0 * M * xq.hidden * 3 * xq.H * xq.D
+    f_out = 2.0 * xo.B * xo.S * xo.H * xo.D * xo.n_out
+
+    def step(ev):
+        ev[0].record(stream)
+        mha.mha_qkv_proj(X, Wqkv, xq.H, xq.D, Q=Q, K=K, V=V, stream=stream)
+        ev[1].record(stream)
+        mha.mha_out_proj(O, Wo, Y=Y, stream=stream)
+        ev[2].record(stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    barrier()
+    if mha.mha_get_device_status(stream) != 0:
+        raise RuntimeError("device status after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clock = ClockSampler(local)
+    if not args.profile:
+        clock.start()
+        time.sleep(0.3)
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for ev in evs:
+        step(ev)
+    t1.record(stream)
+    barrier()
+    clocks = clock.stop() if not args.profile else None
+    if mha.mha_get_device_status(stream) != 0:
+        raise RuntimeError("device status after timed region")
+    tq = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    to = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    total = t0.elapsed_time(t1) / 1e3
+    tq, to, total = max_over_ranks([tq, to, total], dist, dev)
+    if rank != 0:
+        return 0
+    K_ = args.steps
+    peak = peaks["bf16_tflops"]
+
+    def roof(name, flops, t):
+        a = flops / (t / K_) / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": peak, "unit": "TFLOP/s",
+                "frac": a / peak, "frac_of_sustained": a / peaks["bf16_tflops_sustained"],
+                "traffic": None, "peak_source": f"bf16_tflops (burst), of {peak_src}",
+                "kernel": name, "us_per_launch": 1e6 * t / K_}
+
+    line = {"impl": "ours", "metric": "attention projections TFLOP/s (% BF16 peak)",
+            "value": whole_job_rate(world, K_ * (f_qkv + f_out), tq + to) / 1e12,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": K_, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / K_, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{QKV_WORKLOAD} + {OUTPROJ_WORKLOAD}",
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}",
+                       "qkv": {"M": M, "K": xq.hidden, "N": 3 * xq.H * xq.D, "flops": f_qkv},
+                       "out": {"M": xo.B * xo.S, "K": xo.H * xo.D, "N": xo.n_out,
+                               "flops": f_out}},
+            "roofline": roof("qkv_proj_kernel", f_qkv, tq),
+            "out_proj": roof("out_proj_kernel", f_out, to),
+            "clocks": clocks, "gpu_launches": 2 * K_}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--only", choices=("both", "prefill", "decode"), default="both")
+    ap.add_argument("--only", choices=("both", "prefill", "decode", "projections"),
+                    default="both")
     ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
                     choices=[k for k, w in si.WORKLOADS.items()
                              if w["kind"] == "prefill" and w["dtype"] in ("bf16", "f16")],
@@ -502,6 +605,8 @@ def main():
         tdist.init_process_group("nccl")
         dist = tdist
     try:
+        if args.only == "projections":
+            return run_projections(args, rank, world, dist)
         return run_ours(args, rank, world, dist)
     finally:
         if dist is not None:

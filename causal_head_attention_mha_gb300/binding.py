@@ -59,6 +59,8 @@ def _declare(lib):
     lib.mha_decode_noalloc.restype = i
     lib.mha_qkv_proj.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.mha_qkv_proj.restype = i
+    lib.mha_out_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.mha_out_proj.restype = i
     lib.mha_decode_num_splits.argtypes = [i, i]
     lib.mha_decode_num_splits.restype = i
     lib.mha_get_device_status.argtypes = [vp]
@@ -258,6 +260,28 @@ def mha_qkv_proj(X, W, H: int, D: int, Q=None, K=None, V=None, stream=None):
     if st != MHA_OK:
         raise MHAError(st, "mha_qkv_proj")
     return tuple(out)
+
+
+def mha_out_proj(O, W, Y=None, stream=None):
+    """Output projection Y = concat_h(O_h) W_O, bf16; O [B, H, S, D], W [H*D, n_out];
+    returns Y [B, S, n_out].  See include/mha.h: mha_out_proj."""
+    if O.dim() != 4:
+        raise ValueError("O must be [B, H, S, D]")
+    B, H, S, D = O.shape
+    dev = O.device
+    _check(O, "O", torch.bfloat16, (B, H, S, D), dev)
+    if W.dim() != 2 or W.shape[0] != H * D:
+        raise ValueError("W must be [H*D, n_out]")
+    n_out = W.shape[1]
+    _check(W, "W", torch.bfloat16, (H * D, n_out), dev)
+    if Y is None:
+        Y = torch.empty((B, S, n_out), dtype=torch.bfloat16, device=dev)
+    _check(Y, "Y", torch.bfloat16, (B, S, n_out), dev)
+    st = _load().mha_out_proj(O.data_ptr(), W.data_ptr(), Y.data_ptr(), B, H, S, D, n_out,
+                              _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, "mha_out_proj")
+    return Y
 
 
 def mha_decode_num_splits(B: int, H: int) -> int:

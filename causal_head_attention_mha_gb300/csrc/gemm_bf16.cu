@@ -85,6 +85,16 @@ __device__ __forceinline__ void umma_ss_kmajor_mnmajor_x4(uint32_t d_tmem, uint6
                : "memory");
 }
 
+// 4-D tiled TMA load of box (x, y, z, w) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // 2-D tiled TMA load of box (x, y) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
@@ -116,10 +126,17 @@ struct TileMap {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-    qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                    uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
-                    int M, int N, int Kd, int S, int H, int D, uint64_t wait_limit_ns) {
+// The GEMM body.  OUT = false: the Q/K/V projection (A = X [M][Kd] flat,
+// row tiles of 128 rows of B*S, epilogue into Q, K, V [B, H, S, D]).
+// OUT = true: the output projection (A = the attention output O [B, H, S, D]
+// read through a 4-D map as rows (b, s) and columns h*D + d, row tiles of 128
+// positions of one sequence; epilogue into Y [B, S, N] row-major).
+template <bool OUT>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmW,
+                                          uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko,
+                                          uint16_t* __restrict__ Vo, int tiles_m, int M, int N,
+                                          int Kd, int S, int H, int D, int sblocks,
+                                          uint64_t wait_limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -153,14 +170,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{wait_limit_ns, &g_err_gemm_bf16, abort_flag};
-  const TileMap tmap{(M + GM - 1) / GM, (N + GN - 1) / GN};
+  const TileMap tmap{tiles_m, (N + GN - 1) / GN};
   const int ntiles = tmap.tiles_m * tmap.tiles_n;
   const int nk = (Kd + GK - 1) / GK;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&tmX);
+      prefetch_tensormap(&tmA);
       prefetch_tensormap(&tmW);
       int n = 0;
       bool ok = true;
@@ -177,8 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = sbase + st * STAGE_BYTES;
           const uint32_t full = bar(B_FULL + st);
           mbar_arrive_expect_tx(full, STAGE_BYTES);
-          // X viewed as [M][Kd]: rows mt*128.., columns kb*64..
-          tma_load_2d(dst, &tmX, full, kb * GK, mt * GM);
+          if constexpr (OUT) {
+            // O viewed as (d, s, h, b): positions sb*128.. of sequence b,
+            // columns kb*64.. = features (kb*64) % D.. of head (kb*64) / D
+            const int b = mt / sblocks, sb = mt - b * sblocks, k0 = kb * GK;
+            tma_load_4d(dst, &tmA, full, k0 % D, sb * GM, k0 / D, b);
+          } else {
+            // X viewed as [M][Kd]: rows mt*128.., columns kb*64..
+            tma_load_2d(dst, &tmA, full, kb * GK, mt * GM);
+          }
           // W viewed as [Kd][N]: four 64-column blocks of rows kb*64..
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -249,20 +273,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int mt, nt;
       tmap.get(t, mt, nt);
-      const int m = mt * GM + r;
-      const int b = m / S, s = m - (m / S) * S;
+      int b, s;
+      bool row_ok;
+      if constexpr (OUT) {
+        b = mt / sblocks;
+        s = (mt - b * sblocks) * GM + r;
+        row_ok = s < S;
+      } else {
+        const int m = mt * GM + r;
+        row_ok = m < M;
+        b = m / S;
+        s = m - b * S;
+      }
 #pragma unroll 1
       for (int c = 0; c < GN / 32; ++c) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(buf) * GN + c * 32, o);
         const int n0 = nt * GN + c * 32;
-        // N = 3*H*D is a multiple of 32 and D of 32: a 32-column chunk lies in
-        // one head of one of Q, K, V, or entirely past N
-        if (m < M && n0 < N) {
-          const int which = n0 / HD, rem = n0 - which * HD;
-          const int h = rem / D, d0 = rem - h * D;
-          uint16_t* base = which == 0 ? Qo : (which == 1 ? Ko : Vo);
-          uint16_t* dst = base + ((static_cast<size_t>(b) * H + h) * S + s) * D + d0;
+        // N is a multiple of 32 (and so is D): a 32-column chunk lies inside N
+        // (for Q/K/V inside one head of one of them) or entirely past it
+        if (row_ok && n0 < N) {
+          uint16_t* dst;
+          if constexpr (OUT) {
+            dst = Qo + (static_cast<size_t>(b) * S + s) * N + n0;
+          } else {
+            const int which = n0 / HD, rem = n0 - which * HD;
+            const int h = rem / D, d0 = rem - h * D;
+            uint16_t* base = which == 0 ? Qo : (which == 1 ? Ko : Vo);
+            dst = base + ((static_cast<size_t>(b) * H + h) * S + s) * D + d0;
+          }
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -283,6 +322,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
+                    int M, int N, int Kd, int S, int H, int D, uint64_t wait_limit_ns) {
+  gemm_body<false>(tmX, tmW, Qo, Ko, Vo, (M + GM - 1) / GM, M, N, Kd, S, H, D, 0, wait_limit_ns);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    out_proj_kernel(const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmW,
+                    uint16_t* __restrict__ Y, int B, int N, int Kd, int S, int D,
+                    uint64_t wait_limit_ns) {
+  const int sblocks = (S + GM - 1) / GM;
+  gemm_body<true>(tmO, tmW, Y, nullptr, nullptr, B * sblocks, 0, N, Kd, S, 0, D, sblocks,
+                  wait_limit_ns);
 }
 
 // ---------------------------------------------------------------- host side
@@ -320,7 +375,42 @@ bool encode_2d(CUtensorMap* map, const void* ptr, long long rows, long long cols
   return r == CUDA_SUCCESS;
 }
 
+// The attention output O [B][H][S][D] as a 4-D tensor (d, s, h, b), 128-byte
+// swizzle, box = 64 features x 128 positions of one head of one sequence.
+bool encode_bhsd_4d(CUtensorMap* map, const void* ptr, int B, int H, int S, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2,
+                           static_cast<cuuint64_t>(H) * S * D * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(GM), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D,
+                            int n_out, cudaStream_t stream, uint64_t wait_limit_ns) {
+  const int Kd = H * D, N = n_out;
+  CUtensorMap mo, mw;
+  if (!encode_bhsd_4d(&mo, O, B, H, S, D) || !encode_2d(&mw, W, Kd, N, 64, GK))
+    return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(out_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>(B) * ((S + GM - 1) / GM) * ((N + GN - 1) / GN);
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  const unsigned grid = static_cast<unsigned>(tiles < nsm ? tiles : nsm);
+  out_proj_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(mo, mw, static_cast<uint16_t*>(Y), B, N,
+                                                          Kd, S, D, wait_limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B, int S,
                             int hidden, int H, int D, cudaStream_t stream,

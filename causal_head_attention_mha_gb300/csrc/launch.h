@@ -41,6 +41,11 @@ cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void
                             int hidden, int H, int D, cudaStream_t stream,
                             uint64_t wait_limit_ns);
 
+// Output projection Y = concat_h(O_h) W_O: O [B, H, S, D], W [H*D][n_out] row-major,
+// Y [B, S, n_out] row-major, bf16.
+cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D,
+                            int n_out, cudaStream_t stream, uint64_t wait_limit_ns);
+
 // Read and clear the device error word of the prefill / projection translation unit.
 cudaError_t take_prefill_bf16_error(unsigned int* word);
 cudaError_t take_gemm_bf16_error(unsigned int* word);

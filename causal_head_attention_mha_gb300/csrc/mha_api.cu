@@ -183,6 +183,22 @@ int mha_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B,
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
 }
 
+int mha_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D, int n_out,
+                 void* stream) {
+  if (!O || !W || !Y) return MHA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || D < 1 || n_out < 1) return MHA_ERR_INVALID_ARG;
+  const long long M = static_cast<long long>(B) * S, Kd = static_cast<long long>(H) * D;
+  if (M * Kd >= (1LL << 31) || Kd * n_out >= (1LL << 31) || M * n_out >= (1LL << 31))
+    return MHA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return MHA_ERR_UNSUPPORTED;
+  if (n_out % 32 != 0) return MHA_ERR_UNSUPPORTED;  // 32-column store chunks
+  if (!aligned16(O) || !aligned16(W) || !aligned16(Y)) return MHA_ERR_MISALIGNED;
+  const cudaError_t e = mha::launch_out_proj(O, W, Y, B, H, S, D, n_out,
+                                             static_cast<cudaStream_t>(stream),
+                                             g_wait_limit_ns.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
 int mha_decode_num_splits(int B, int H) {
   if (B < 1 || H < 1) return 0;
   const int nsm = mha::device_sm_count();

@@ -197,6 +197,22 @@ int mha_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B,
                  int hidden, int H, int D, void* stream);
 
 /*
+ * Output projection after attention (page 1 section 2.1 lists it as one more
+ * GEMM): the heads of O are concatenated, feature h*D + d of row (b, s) being
+ * O[b][h][s][d], and multiplied by W_O.  This is also the per-head grouped
+ * form Y = sum_h O_h W_O[h*D:(h+1)*D], summed in one fp32 accumulator.
+ * bf16 in and out, tensor cores.
+ *
+ *   O       : const bf16 [B, H, S, D] (the layout mha_fwd writes).
+ *   W       : const bf16 [H*D, n_out], row-major.
+ *   Y       : bf16 [B, S, n_out], row-major, written.
+ *   D : 64 or 128.   n_out : >= 1 and a multiple of 32.
+ *   B*S*H*D, H*D*n_out and B*S*n_out each < 2^31.
+ */
+int mha_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D, int n_out,
+                 void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * bounded waits set.  Returns MHA_OK, MHA_ERR_TIMEOUT when a wait in some
  * kernel of this library ran out since the last call, or MHA_ERR_CUDA when

@@ -162,6 +162,26 @@ def projection_inputs(B: int, S: int, hidden: int, H: int, D: int, seed: int) ->
         B, S, hidden, H, D)
 
 
+@dataclass
+class OutProjectionInputs:
+    O: Tensor   # [B, H, S, D], attention output layout
+    W: Tensor   # [H*D, n_out] = W_O
+    B: int
+    H: int
+    S: int
+    D: int
+    n_out: int
+
+
+def out_projection_inputs(B: int, H: int, S: int, D: int, n_out: int,
+                          seed: int) -> OutProjectionInputs:
+    """O ~ N(0, 1) and W ~ N(0, 1/(H*D)) (outputs of order one), bf16."""
+    return OutProjectionInputs(
+        make_tensor(seed, STREAM_Q, (B, H, S, D), 1.0, "bf16"),
+        make_tensor(seed, STREAM_V, (H * D, n_out), 1.0 / math.sqrt(H * D), "bf16"),
+        B, H, S, D, n_out)
+
+
 # The five synthetic workloads (shapes, distributions and seeds), then the
 # same bench shapes on f16 data.
 WORKLOADS = {
@@ -183,6 +203,10 @@ WORKLOADS = {
     # layer: hidden 4096 = 32 heads x 128)
     "qkv_bf16_b4s4096hid4096_h32d128": dict(kind="projection", B=4, S=4096, hidden=4096, H=32,
                                             D=128, seed=1009),
+    # the output projection after the bench's attention shape (concatenated
+    # 32 x 128 heads times W_O [4096, 4096])
+    "outproj_bf16_b4h32s4096d128_n4096": dict(kind="out_projection", B=4, H=32, S=4096, D=128,
+                                              n_out=4096, seed=1010),
     # key padding: the bench shape with per-sequence key lengths U{1024..4096}
     "prefill_varlen_bf16_b4h32s4096d128": dict(kind="prefill", B=4, H=32, S=4096, D=128,
                                                dtype="bf16", qk_std=1.0, seed=1008,
@@ -193,6 +217,8 @@ WORKLOADS = {
 
 def workload_inputs(name: str):
     w = WORKLOADS[name]
+    if w["kind"] == "out_projection":
+        return out_projection_inputs(w["B"], w["H"], w["S"], w["D"], w["n_out"], w["seed"])
     if w["kind"] == "projection":
         return projection_inputs(w["B"], w["S"], w["hidden"], w["H"], w["D"], w["seed"])
     if w["kind"] == "prefill":

@@ -145,3 +145,16 @@ def test_qkv_proj_validation(lib, kw, expected):
     a.update(kw)
     assert lib.mha_qkv_proj(a["X"], a["W"], a["Q"], a["K"], a["V"], a["B"], a["S"], a["hidden"],
                             a["H"], a["D"], None) == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(O=None), INVALID), (dict(Y=None), INVALID), (dict(B=0), INVALID), (dict(S=0), INVALID),
+    (dict(n_out=0), INVALID), (dict(B=1 << 12, S=1 << 12, H=64), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(n_out=48), UNSUPPORTED),
+    (dict(W=FAKE + 8), MISALIGNED), (dict(Y=FAKE + 2), MISALIGNED),
+])
+def test_out_proj_validation(lib, kw, expected):
+    a = dict(O=FAKE, W=FAKE, Y=FAKE, B=1, H=2, S=128, D=64, n_out=256)
+    a.update(kw)
+    assert lib.mha_out_proj(a["O"], a["W"], a["Y"], a["B"], a["H"], a["S"], a["D"], a["n_out"],
+                            None) == expected
