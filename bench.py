@@ -117,6 +117,14 @@ def whole_job_rate(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
+def launch_percentiles(ms_list):
+    """p50 / p95 of per-launch device times given in ms, returned in us."""
+    v = sorted(ms_list)
+    def q(f):
+        return 1e3 * v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
+    return {"us_p50": q(0.5), "us_p95": q(0.95)}
+
+
 def prefill_flops(B, H, S, D, causal=True):
     return (2.0 if causal else 4.0) * B * H * S * S * D
 
@@ -440,7 +448,8 @@ def run_ours(args, rank, world, dist):
                     "traffic": traffic_for("prefill_" + pdt, args.prefill_workload),
                     "peak_source": f"bf16_tflops (burst), of {peak_src}",
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "kernel": f"prefill_{pdt}{'_varlen' if varlen else ''}_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s}
+                    "kernel": f"prefill_{pdt}{'_varlen' if varlen else ''}_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s,
+                    **launch_percentiles([e[0].elapsed_time(e[1]) for e in evs])}
         line["roofline"] = roofline
     if do_decode:
         gbs = whole_job_rate(world, K_ * dbytes, td) / 1e9
@@ -451,7 +460,8 @@ def run_ours(args, rank, world, dist):
                           "achieved": dbytes / (td / K_) / 1e9, "peak": peaks["hbm_gbs"],
                           "frac": dbytes / (td / K_) / 1e9 / peaks["hbm_gbs"],
                           "traffic": traffic_for("decode", args.decode_workload), "peak_source": f"hbm_gbs, of {peak_src}",
-                          "us_per_call": 1e6 * td / K_}
+                          "us_per_call": 1e6 * td / K_,
+                          **launch_percentiles([e[1].elapsed_time(e[2]) for e in evs])}
         if not do_prefill:
             line.update({"value": gbs, "unit": "GB/s"})
     line.update({
@@ -544,12 +554,13 @@ def run_projections(args, rank, world, dist):
     K_ = args.steps
     peak = peaks["bf16_tflops"]
 
-    def roof(name, flops, t):
+    def roof(name, flops, t, j):
         a = flops / (t / K_) / 1e12
         return {"bound": "tensor", "achieved": a, "peak": peak, "unit": "TFLOP/s",
                 "frac": a / peak, "frac_of_sustained": a / peaks["bf16_tflops_sustained"],
                 "traffic": None, "peak_source": f"bf16_tflops (burst), of {peak_src}",
-                "kernel": name, "us_per_launch": 1e6 * t / K_}
+                "kernel": name, "us_per_launch": 1e6 * t / K_,
+                **launch_percentiles([e[j].elapsed_time(e[j + 1]) for e in evs])}
 
     line = {"impl": "ours", "metric": "attention projections TFLOP/s (% BF16 peak)",
             "value": whole_job_rate(world, K_ * (f_qkv + f_out), tq + to) / 1e12,
@@ -562,8 +573,8 @@ def run_projections(args, rank, world, dist):
                        "qkv": {"M": M, "K": xq.hidden, "N": 3 * xq.H * xq.D, "flops": f_qkv},
                        "out": {"M": xo.B * xo.S, "K": xo.H * xo.D, "N": xo.n_out,
                                "flops": f_out}},
-            "roofline": roof("qkv_proj_kernel", f_qkv, tq),
-            "out_proj": roof("out_proj_kernel", f_out, to),
+            "roofline": roof("qkv_proj_kernel", f_qkv, tq, 0),
+            "out_proj": roof("out_proj_kernel", f_out, to, 1),
             "clocks": clocks, "gpu_launches": 2 * K_}
     print(json.dumps(line), flush=True)
     return 0

@@ -82,3 +82,12 @@ def test_max_over_ranks_single_process_is_identity():
     import bench
     assert bench.max_over_ranks([0.5, 2.0], None, torch.device("cpu")) == [0.5, 2.0]
     assert bench.whole_job_rate(1, 10.0, 2.0) == 5.0
+
+
+def test_launch_percentiles_nearest_rank():
+    import bench
+    p = bench.launch_percentiles([0.4, 0.1, 0.3, 0.2] + [0.25] * 16)
+    assert p["us_p50"] == pytest.approx(250.0)
+    assert p["us_p95"] == pytest.approx(300.0)
+    one = bench.launch_percentiles([0.5])
+    assert one == {"us_p50": 500.0, "us_p95": 500.0}
