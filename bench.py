@@ -62,6 +62,13 @@ TRAFFIC = {
     "decode_f16": {"kernel": "decode", "workload": "decode_f16_b16h32d128_len512_8192",
                    "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                    "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1292623616},
+    # profiles/proj_gemm_bf16_b4s4096_h32d128.md (both projection kernels, one capture)
+    "qkv_proj": {"kernel": "qkv_proj", "workload": "qkv_bf16_b4s4096hid4096_h32d128",
+                 "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                 "sha256": "091235ec9c352f7610ea6693eac7fe6a1da72da38e69c1b3ba8d940a0d7d57ba", "bytes_per_launch": 1313714176},
+    "out_proj": {"kernel": "out_proj", "workload": "outproj_bf16_b4h32s4096d128_n4096",
+                 "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                 "sha256": "091235ec9c352f7610ea6693eac7fe6a1da72da38e69c1b3ba8d940a0d7d57ba", "bytes_per_launch": 382867968},
 }
 
 
@@ -554,11 +561,11 @@ def run_projections(args, rank, world, dist):
     K_ = args.steps
     peak = peaks["bf16_tflops"]
 
-    def roof(name, flops, t, j):
+    def roof(name, flops, t, j, traffic):
         a = flops / (t / K_) / 1e12
         return {"bound": "tensor", "achieved": a, "peak": peak, "unit": "TFLOP/s",
                 "frac": a / peak, "frac_of_sustained": a / peaks["bf16_tflops_sustained"],
-                "traffic": None, "peak_source": f"bf16_tflops (burst), of {peak_src}",
+                "traffic": traffic, "peak_source": f"bf16_tflops (burst), of {peak_src}",
                 "kernel": name, "us_per_launch": 1e6 * t / K_,
                 **launch_percentiles([e[j].elapsed_time(e[j + 1]) for e in evs])}
 
@@ -573,8 +580,9 @@ def run_projections(args, rank, world, dist):
                        "qkv": {"M": M, "K": xq.hidden, "N": 3 * xq.H * xq.D, "flops": f_qkv},
                        "out": {"M": xo.B * xo.S, "K": xo.H * xo.D, "N": xo.n_out,
                                "flops": f_out}},
-            "roofline": roof("qkv_proj_kernel", f_qkv, tq, 0),
-            "out_proj": roof("out_proj_kernel", f_out, to, 1),
+            "roofline": roof("qkv_proj_kernel", f_qkv, tq, 0, traffic_for("qkv_proj", QKV_WORKLOAD)),
+            "out_proj": roof("out_proj_kernel", f_out, to, 1,
+                             traffic_for("out_proj", OUTPROJ_WORKLOAD)),
             "clocks": clocks, "gpu_launches": 2 * K_}
     print(json.dumps(line), flush=True)
     return 0
