@@ -1,26 +1,41 @@
-// gemm_bf16.cu — the fused Q, K, V projection on the sm_103a tensor cores
-// (tcgen05 + TMEM) fed by TMA, bf16 in and out, fp32 accumulation.
+// gemm_bf16.cu — the Q/K/V projection and the output projection around
+// attention, on the sm_103a tensor cores (tcgen05 + TMEM) fed by TMA, bf16 in
+// and out, fp32 accumulation.
 //
-// Method: page "Hand-written masked multi-head attention CUDA kernel:
-// underlying logic and practice" section 2 (Q = X W_Q, K = X W_K,
-// V = X W_V) with the shapes of its section 2.1 (X: batch x seq_len x
-// hidden; each W: hidden x heads*head_dim).  Page "Week 4 CUDA notes"
-// section 2.1 fuses the three products into one GEMM: W = [W_Q | W_K | W_V]
-// (hidden x 3*H*D), Y = X W, and Y is written straight into Q, K and V in the
-// [B, H, S, D] layout the attention kernels read (column n = c*H*D + h*D + d
-// of Y is feature d of head h of Q, K or V for c = 0, 1, 2).
+// Methods:
+// - Q/K/V: page "Hand-written masked multi-head attention CUDA kernel:
+//   underlying logic and practice" section 2 (Q = X W_Q, K = X W_K,
+//   V = X W_V) with the shapes of its section 2.1 (X: batch x seq_len x
+//   hidden; each W: hidden x heads*head_dim).  Page "Week 4 CUDA notes"
+//   section 2.1 fuses the three products into one GEMM: W = [W_Q | W_K | W_V]
+//   (hidden x 3*H*D), Y = X W, written straight into Q, K and V in the
+//   [B, H, S, D] layout the attention kernels read (column n = c*H*D + h*D + d
+//   of Y is feature d of head h of Q, K or V for c = 0, 1, 2).
+// - Output projection: the same page's section 2.1 lists it after attention
+//   as one more GEMM, Y = concat_h(O_h) W_O; A is read from O [B, H, S, D]
+//   through a 4-D view (d, s, h, b), so row (b, s) and column h*D + d of the
+//   concatenation come from O without a transpose.
 //
-// Tiles of 128 rows (M = B*S) x 256 columns (N = 3*H*D); K (= hidden) in
-// steps of 64 through a ring of 4 stages, each the 128 x 64 slice of X
-// (K-major, 16 KB) and the 64 x 256 slice of W (MN-major: four 64-column
-// blocks of 8 KB), both 128-byte swizzled.  A persistent grid walks the
-// tiles in groups of 16 row tiles, all column tiles of a group before the
-// next, so a W slice is reused by the group while it is in L2.  Roles:
-//   warp 0       TMA producer of the ring
-//   warp 1       tensor-memory allocation; one thread issues every MMA
-//                (M = 128, N = 256, K = 16; fp32 accumulator in TMEM)
+// Each output tile of 256 rows x 256 columns belongs to a pair of CTAs (a
+// cluster of 2 on two SMs): one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 with M = 256, N = 256, K = 16, where each CTA
+// holds its own 128 rows of A and one half (128 columns) of W's slice, and
+// each CTA's tensor memory receives its 128 rows of the fp32 accumulator.
+// Sharing W across the pair halves the W bytes each SM fetches per output.
+// K runs in steps of 64 through a ring of 6 stages per CTA, each the
+// 128 x 64 slice of A (K-major, 16 KB) and a 64 x 128 slice of W (MN-major:
+// two 64-column blocks of 8 KB), both 128-byte swizzled; both CTAs' copies
+// of a stage complete on the even CTA's barrier.  A persistent grid of
+// pairs walks the tiles in groups of 8 row tiles, all column tiles of a
+// group before the next, so a W slice is reused by the group while it is in
+// L2.  Roles in each CTA:
+//   warp 0       TMA producer of its half of the ring
+//   warp 1       tensor-memory allocation (both CTAs together); in the even
+//                CTA one thread issues every MMA and its commits, which
+//                arrive on the barriers of both CTAs
 //   warps 4..7   epilogue: one output row per thread, TMEM -> bf16 ->
-//                16-byte stores into Q, K, V
+//                16-byte stores; each warp then tells the even CTA that its
+//                rows of the accumulator are free
 // The accumulator is double-buffered (2 x 256 TMEM columns): the epilogue of
 // one tile overlaps the products of the next.  Every wait is bounded in time
 // (an expired wait sets this unit's error word and the CTA winds down).
@@ -35,22 +50,21 @@ __device__ unsigned int g_err_gemm_bf16 = 0;
 
 namespace {
 
-constexpr int GM = 128, GN = 256, GK = 64;
-constexpr int kStages = 4;
-constexpr int kGroupM = 16;                    // row tiles per scheduling group
+constexpr int GM = 128, GN = 256, GK = 64;     // GM rows per CTA, 2 * GM per pair
+constexpr int kStages = 6;
+constexpr int kGroupM = 8;                     // pair row tiles per scheduling group
 constexpr int A_BYTES = GM * GK * 2;           // 16 KB
 constexpr int B_BLOCK = GK * 64 * 2;           // one 64-column block of W: 8 KB
-constexpr int B_BYTES = 4 * B_BLOCK;           // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int B_BYTES = 2 * B_BLOCK;           // this CTA's 128 columns: 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
 constexpr int BAR_OFF = kStages * STAGE_BYTES;
-// barrier indices
-constexpr int B_FULL = 0;                  // [stage] its tiles landed
-constexpr int B_EMPTY = B_FULL + kStages;  // [stage] its last MMA complete
-constexpr int B_AFULL = B_EMPTY + kStages;  // [buffer] the tile's accumulator is final
-constexpr int B_AFREE = B_AFULL + 2;        // [buffer] the epilogue has read it (128 arrivals)
+constexpr int B_FULL = 0;                   // [stage] both CTAs' tiles landed (leader's copy used)
+constexpr int B_EMPTY = B_FULL + kStages;   // [stage] its last MMA complete (both CTAs)
+constexpr int B_AFULL = B_EMPTY + kStages;  // [buffer] the tile's accumulator is final (both CTAs)
+constexpr int B_AFREE = B_AFULL + 2;        // [buffer] both epilogues read it (leader, 8 arrivals)
 constexpr int B_DRAIN = B_AFREE + 2;
 constexpr int NBAR = B_DRAIN + 1;
-constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // barriers + flags, alignment slack
+constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
 constexpr int kThreads = 256;
 constexpr int kEpiWarp0 = 4;
 static_assert(NBAR * 8 + 8 <= 256, "barrier area");
@@ -58,50 +72,89 @@ static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 enum : uint32_t { GSITE_PROD_EMPTY = 1, GSITE_MMA_FULL, GSITE_MMA_AFREE, GSITE_EPI_AFULL };
 
-// 4 MMAs D += A B over K = 64, both operands in shared memory: A K-major
-// (128-byte swizzle: the next 16 k are 32 bytes further, +2 in the
-// descriptor's address field), B MN-major (the next 16 k are 16 rows =
-// 2048 bytes further, +128).
-__device__ __forceinline__ void umma_ss_kmajor_mnmajor_x4(uint32_t d_tmem, uint64_t adesc,
-                                                          uint64_t bdesc, uint32_t idesc,
-                                                          uint32_t acc_first) {
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the shared::cluster address of the same shared variable in CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// arrive once on `bar` (same offset) in every CTA of `mask` when the MMAs
+// this thread issued so far are complete
+__device__ __forceinline__ void umma_commit2_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// 4 MMAs over K = 64 on the pair: A K-major (+32 B per 16 k), B MN-major
+// (+16 rows = 2048 B per 16 k); each CTA supplies its rows of A and its half
+// of B's columns at the same shared-memory offsets.
+__device__ __forceinline__ void umma2_ss_kmajor_mnmajor_x4(uint32_t d_tmem, uint64_t adesc,
+                                                           uint64_t bdesc, uint32_t idesc,
+                                                           uint32_t acc_first) {
   asm volatile("{\n\t"
                ".reg .pred pf, pt;\n\t"
                ".reg .b64 a, b;\n\t"
                "setp.ne.b32 pf, %4, 0;\n\t"
                "setp.eq.b32 pt, %4, %4;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, pf;\n\t"
                "add.s64 a, %1, 2;\n\t"
                "add.s64 b, %2, 128;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
                "add.s64 a, %1, 4;\n\t"
                "add.s64 b, %2, 256;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
                "add.s64 a, %1, 6;\n\t"
                "add.s64 b, %2, 384;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
                "}" ::"r"(d_tmem),
                "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc_first)
                : "memory");
 }
 
-// 4-D tiled TMA load of box (x, y, z, w) into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z, int w) {
+// TMA loads whose completion is counted on the pair leader's barrier
+// (`bar` a shared::cluster address); the data lands in this CTA.
+__device__ __forceinline__ void tma2_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int x, int y) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
-
-// 2-D tiled TMA load of box (x, y) into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 
@@ -112,8 +165,8 @@ __device__ __forceinline__ void st_global_v4_g(void* p, uint32_t a, uint32_t b, 
                : "memory");
 }
 
-// Tile t of the persistent walk -> (row tile, column tile): groups of
-// kGroupM row tiles, column tiles outer within a group.
+// Pair tile t -> (row tile of 256 rows, column tile): groups of kGroupM row
+// tiles, column tiles outer within a group.
 struct TileMap {
   int tiles_m, tiles_n;
   __device__ void get(int t, int& mt, int& nt) const {
@@ -126,11 +179,6 @@ struct TileMap {
   }
 };
 
-// The GEMM body.  OUT = false: the Q/K/V projection (A = X [M][Kd] flat,
-// row tiles of 128 rows of B*S, epilogue into Q, K, V [B, H, S, D]).
-// OUT = true: the output projection (A = the attention output O [B, H, S, D]
-// read through a 4-D map as rows (b, s) and columns h*D + d, row tiles of 128
-// positions of one sequence; epilogue into Y [B, S, N] row-major).
 template <bool OUT>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmW,
                                           uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko,
@@ -142,6 +190,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
@@ -155,33 +205,35 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_AFULL + b), 1);
-      mbar_init(bar(B_AFREE + b), 128);
+      mbar_init(bar(B_AFREE + b), 8);  // one per epilogue warp of both CTAs
     }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc2(smem_addr(tmem_slot), 512);
+    tmem_relinquish2();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{wait_limit_ns, &g_err_gemm_bf16, abort_flag};
   const TileMap tmap{tiles_m, (N + GN - 1) / GN};
   const int ntiles = tmap.tiles_m * tmap.tiles_n;
   const int nk = (Kd + GK - 1) / GK;
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       prefetch_tensormap(&tmA);
       prefetch_tensormap(&tmW);
+      const uint32_t full_leader = mapa_shared(bar(B_FULL), 0);
       int n = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      for (int t = pair; ok && t < ntiles; t += npairs) {
         int mt, nt;
         tmap.get(t, mt, nt);
         for (int kb = 0; kb < nk; ++kb, ++n) {
@@ -192,25 +244,29 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             break;
           }
           const uint32_t dst = sbase + st * STAGE_BYTES;
-          const uint32_t full = bar(B_FULL + st);
-          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          const uint32_t full = full_leader + 8u * st;
+          // the leader's barrier counts both CTAs' bytes of this stage
+          if (leader) mbar_arrive_expect_tx(bar(B_FULL + st), 2 * STAGE_BYTES);
           if constexpr (OUT) {
-            // O viewed as (d, s, h, b): positions sb*128.. of sequence b,
-            // columns kb*64.. = features (kb*64) % D.. of head (kb*64) / D
             const int b = mt / sblocks, sb = mt - b * sblocks, k0 = kb * GK;
-            tma_load_4d(dst, &tmA, full, k0 % D, sb * GM, k0 / D, b);
+            tma2_load_4d(dst, &tmA, full, k0 % D, sb * 2 * GM + static_cast<int>(rank) * GM,
+                         k0 / D, b);
           } else {
-            // X viewed as [M][Kd]: rows mt*128.., columns kb*64..
-            tma_load_2d(dst, &tmA, full, kb * GK, mt * GM);
+            tma2_load_2d(dst, &tmA, full, kb * GK, mt * 2 * GM + static_cast<int>(rank) * GM);
           }
-          // W viewed as [Kd][N]: four 64-column blocks of rows kb*64..
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_load_2d(dst + A_BYTES + j * B_BLOCK, &tmW, full, nt * GN + j * 64, kb * GK);
+          for (int j = 0; j < 2; ++j)
+            tma2_load_2d(dst + A_BYTES + j * B_BLOCK, &tmW, full,
+                         nt * GN + static_cast<int>(rank) * 128 + j * 64, kb * GK);
         }
       }
-      if (*abort_flag) {
-        // let every copy still in flight land before the CTA can exit
+      if (ok) {
+        // every stage's last release (a commit from the leader) has landed here
+        for (int st = 0; st < kStages && st < n; ++st) {
+          const int last = st + ((n - 1 - st) / kStages) * kStages;
+          if (!mbar_wait(bar(B_EMPTY + st), (last / kStages) & 1, wc, GSITE_PROD_EMPTY)) break;
+        }
+      } else if (leader) {
         for (int st = 0; st < kStages && st < n; ++st) {
           const int last = st + ((n - 1 - st) / kStages) * kStages;
           mbar_wait_drain(bar(B_FULL + st), (last / kStages) & 1, kDrainLimitNs);
@@ -219,19 +275,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(GM, GN, true);
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * GM, GN, true);
       const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(0, 0, 1024) >> 32);
       auto desc = [&](uint32_t lo) { return (static_cast<uint64_t>(desc_hi) << 32) | lo; };
-      // A: K-major, LBO unused; B: MN-major, LBO = the next 64-column block
       const uint32_t a_lo0 = (sbase >> 4) | (1u << 16);
       const uint32_t b_lo0 = ((sbase + A_BYTES) >> 4) | ((B_BLOCK >> 4) << 16);
       int n = 0, tc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++tc) {
+      for (int t = pair; ok && t < ntiles; t += npairs, ++tc) {
         const int buf = tc & 1;
-        // the epilogue has read this buffer's previous tile
         if (tc >= 2 && !mbar_wait(bar(B_AFREE + buf), ((tc >> 1) - 1) & 1, wc, GSITE_MMA_AFREE)) {
           ok = false;
           break;
@@ -246,30 +300,29 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           }
           tc_fence_after();
           const uint32_t off = static_cast<uint32_t>(st * STAGE_BYTES) >> 4;
-          umma_ss_kmajor_mnmajor_x4(dtm, desc(a_lo0 + off), desc(b_lo0 + off), idesc,
-                                    kb > 0 ? 1u : 0u);
-          umma_commit(bar(B_EMPTY + st));  // the stage is free once these MMAs complete
+          umma2_ss_kmajor_mnmajor_x4(dtm, desc(a_lo0 + off), desc(b_lo0 + off), idesc,
+                                     kb > 0 ? 1u : 0u);
+          umma_commit2_mc(bar(B_EMPTY + st), 3);  // the stage is free in both CTAs
         }
         if (!ok) break;
-        umma_commit(bar(B_AFULL + buf));
+        umma_commit2_mc(bar(B_AFULL + buf), 3);
       }
-      // every MMA issued completes before tensor memory is freed
-      umma_commit(bar(B_DRAIN));
+      umma_commit2_mc(bar(B_DRAIN), 1);
       mbar_wait_drain(bar(B_DRAIN), 0, kDrainLimitNs);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // row of the tile = TMEM lane
+    const int r = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t afree_leader = mapa_shared(bar(B_AFREE), 0);
     const int HD = H * D;
-    bool failed = false;
     int tc = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
+    for (int t = pair; t < ntiles; t += npairs, ++tc) {
       const int buf = tc & 1;
-      failed = !__all_sync(0xffffffffu, mbar_wait(bar(B_AFULL + buf), (tc >> 1) & 1, wc, GSITE_EPI_AFULL));
-      if (failed) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_AFULL + buf), (tc >> 1) & 1, wc, GSITE_EPI_AFULL)))
+        break;
       tc_fence_after();
       int mt, nt;
       tmap.get(t, mt, nt);
@@ -277,10 +330,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       bool row_ok;
       if constexpr (OUT) {
         b = mt / sblocks;
-        s = (mt - b * sblocks) * GM + r;
+        s = (mt - b * sblocks) * 2 * GM + static_cast<int>(rank) * GM + r;
         row_ok = s < S;
       } else {
-        const int m = mt * GM + r;
+        const int m = mt * 2 * GM + static_cast<int>(rank) * GM + r;
         row_ok = m < M;
         b = m / S;
         s = m - b * S;
@@ -290,8 +343,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         uint32_t o[32];
         tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(buf) * GN + c * 32, o);
         const int n0 = nt * GN + c * 32;
-        // N is a multiple of 32 (and so is D): a 32-column chunk lies inside N
-        // (for Q/K/V inside one head of one of them) or entirely past it
         if (row_ok && n0 < N) {
           uint16_t* dst;
           if constexpr (OUT) {
@@ -311,16 +362,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             st_global_v4_g(dst + c4 * 8, w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
         }
       }
-      // the buffer may take the next tile's products
       tc_fence_before();
-      mbar_arrive(bar(B_AFREE + buf));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(afree_leader + 8u * buf);
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // the leader's MMAs are drained; no arrival between the CTAs is pending
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc2(tmem, 512);
   }
 }
 
@@ -328,14 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
                     int M, int N, int Kd, int S, int H, int D, uint64_t wait_limit_ns) {
-  gemm_body<false>(tmX, tmW, Qo, Ko, Vo, (M + GM - 1) / GM, M, N, Kd, S, H, D, 0, wait_limit_ns);
+  gemm_body<false>(tmX, tmW, Qo, Ko, Vo, (M + 2 * GM - 1) / (2 * GM), M, N, Kd, S, H, D, 0,
+                   wait_limit_ns);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     out_proj_kernel(const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmW,
                     uint16_t* __restrict__ Y, int B, int N, int Kd, int S, int D,
                     uint64_t wait_limit_ns) {
-  const int sblocks = (S + GM - 1) / GM;
+  const int sblocks = (S + 2 * GM - 1) / (2 * GM);
   gemm_body<true>(tmO, tmW, Y, nullptr, nullptr, B * sblocks, 0, N, Kd, S, 0, D, sblocks,
                   wait_limit_ns);
 }
@@ -392,6 +444,34 @@ bool encode_bhsd_4d(CUtensorMap* map, const void* ptr, int B, int H, int S, int 
   return r == CUDA_SUCCESS;
 }
 
+// Persistent grid of CTA pairs (clusters of 2), as many pairs as can be
+// resident at once, at most one per pair tile.
+template <typename Kern>
+cudaError_t launch_pairs(Kern kern, long long pair_tiles, cudaStream_t stream,
+                         cudaLaunchConfig_t& cfg, cudaLaunchAttribute& attr) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  cfg.gridDim = dim3(static_cast<unsigned>(nsm & ~1), 1, 1);
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const long long pairs = pair_tiles < max_clusters ? pair_tiles : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D,
@@ -400,15 +480,14 @@ cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H,
   CUtensorMap mo, mw;
   if (!encode_bhsd_4d(&mo, O, B, H, S, D) || !encode_2d(&mw, W, Kd, N, 64, GK))
     return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(out_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const long long tiles = static_cast<long long>(B) * ((S + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr = {};
+  cudaError_t e = launch_pairs(out_proj_kernel, tiles, stream, cfg, attr);
   if (e != cudaSuccess) return e;
-  const long long tiles = static_cast<long long>(B) * ((S + GM - 1) / GM) * ((N + GN - 1) / GN);
-  const int nsm = device_sm_count();
-  if (nsm <= 0) return cudaErrorInvalidDevice;
-  const unsigned grid = static_cast<unsigned>(tiles < nsm ? tiles : nsm);
-  out_proj_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(mo, mw, static_cast<uint16_t*>(Y), B, N,
-                                                          Kd, S, D, wait_limit_ns);
+  uint16_t* y = static_cast<uint16_t*>(Y);
+  e = cudaLaunchKernelEx(&cfg, out_proj_kernel, mo, mw, y, B, N, Kd, S, D, wait_limit_ns);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -419,16 +498,14 @@ cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void
   CUtensorMap mx, mw;
   if (!encode_2d(&mx, X, M, Kd, GK, GM) || !encode_2d(&mw, W, Kd, N, 64, GK))
     return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(qkv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const long long tiles = static_cast<long long>((M + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr = {};
+  cudaError_t e = launch_pairs(qkv_proj_kernel, tiles, stream, cfg, attr);
   if (e != cudaSuccess) return e;
-  const long long tiles = static_cast<long long>((M + GM - 1) / GM) * ((N + GN - 1) / GN);
-  const int nsm = device_sm_count();
-  if (nsm <= 0) return cudaErrorInvalidDevice;
-  const unsigned grid = static_cast<unsigned>(tiles < nsm ? tiles : nsm);
-  qkv_proj_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(
-      mx, mw, static_cast<uint16_t*>(Q), static_cast<uint16_t*>(K), static_cast<uint16_t*>(V), M, N,
-      Kd, S, H, D, wait_limit_ns);
+  uint16_t *q = static_cast<uint16_t*>(Q), *k = static_cast<uint16_t*>(K), *v = static_cast<uint16_t*>(V);
+  e = cudaLaunchKernelEx(&cfg, qkv_proj_kernel, mx, mw, q, k, v, M, N, Kd, S, H, D, wait_limit_ns);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
