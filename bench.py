@@ -65,10 +65,10 @@ TRAFFIC = {
     # profiles/proj_gemm_bf16_b4s4096_h32d128.md (both projection kernels, one capture)
     "qkv_proj": {"kernel": "qkv_proj", "workload": "qkv_bf16_b4s4096hid4096_h32d128",
                  "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                 "sha256": "091235ec9c352f7610ea6693eac7fe6a1da72da38e69c1b3ba8d940a0d7d57ba", "bytes_per_launch": 1313714176},
+                 "sha256": "9d394e353523791f3121bbbb7638f1a7c6dd93b822b862823ba7f5de988572dc", "bytes_per_launch": 1352056576},
     "out_proj": {"kernel": "out_proj", "workload": "outproj_bf16_b4h32s4096d128_n4096",
                  "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                 "sha256": "091235ec9c352f7610ea6693eac7fe6a1da72da38e69c1b3ba8d940a0d7d57ba", "bytes_per_launch": 382867968},
+                 "sha256": "9d394e353523791f3121bbbb7638f1a7c6dd93b822b862823ba7f5de988572dc", "bytes_per_launch": 409215744},
 }
 
 
