@@ -164,34 +164,56 @@ struct ItemShape {
 };
 
 // Static schedule of the work items over a persistent grid, walked
-// identically by every role of a CTA.  Heads are taken in groups small
-// enough that the group's K and V stay in L2 (about two items per CTA per
-// group); inside a group the items are ranked by decreasing work (causal:
-// later query blocks first) and dealt to the CTAs in snake order (0..G-1,
-// then G-1..0, ...), which balances the work of each CTA without any shared
-// counter.
+// identically by every role of a CTA.  Heads are taken in groups whose K and
+// V stay in L2; inside a group the items are ranked by decreasing work
+// (causal: later query blocks first) and dealt to the CTAs in snake order
+// (0..G-1, then G-1..0, ...), which balances the work of each CTA without
+// any shared counter.  Two group shapes:
+//   WIDE = false (D = 128): about two items per CTA per group, the last
+//     group holding whatever heads are left;
+//   WIDE = true (D = 64): about four items per CTA per group, the heads that
+//     would not fill a last group spread over the others (so every group
+//     deals at least G items), and the snake direction carried on from one
+//     group to the next.  On long causal sequences the first shape leaves a
+//     last group of fewer items than CTAs, all of different sizes, and SMs
+//     idle for ~13 % of a launch; at D = 128 the larger groups of the second
+//     shape (twice the K and V in flight) measured slower.
+template <bool WIDE>
 struct Sched {
-  int n_qp, BH, G, c, hg;
+  int n_qp, BH, G, c, ng, base_h, extra;
   bool causal;
-  int group, t;
+  int group, t, rounds;  // rounds dealt in earlier groups (WIDE)
   __device__ Sched(int n_qp_, int BH_, bool causal_)
-      : n_qp(n_qp_), BH(BH_), G(gridDim.x), c(blockIdx.x), causal(causal_), group(0), t(0) {
-    hg = (2 * G + n_qp - 1) / n_qp;
-    if (hg < 1) hg = 1;
+      : n_qp(n_qp_), BH(BH_), G(gridDim.x), c(blockIdx.x), causal(causal_), group(0), t(0),
+        rounds(0) {
+    int target = ((WIDE ? 4 : 2) * G + n_qp - 1) / n_qp;  // heads per group
+    if (target < 1) target = 1;
+    if (WIDE) {
+      ng = BH / target;
+      if (ng < 1) ng = 1;
+      base_h = BH / ng;
+      extra = BH - base_h * ng;
+    } else {
+      ng = (BH + target - 1) / target;
+      base_h = target;
+      extra = 0;
+    }
   }
   __device__ bool next(int& bh, int& qp) {
     while (true) {
-      const int h0 = group * hg;
-      if (h0 >= BH) return false;
-      const int nh = min(hg, BH - h0);
+      if (group >= ng) return false;
+      const int h0 = group * base_h + min(group, extra);
+      const int nh = min(base_h + (group < extra ? 1 : 0), BH - h0);
       const int n = nh * n_qp;
       const int base = t * G;
       if (base >= n) {
         ++group;
+        rounds += t;
         t = 0;
         continue;
       }
-      const int r = base + ((t & 1) ? (G - 1 - c) : c);
+      const int dir = (WIDE ? rounds + t : t) & 1;
+      const int r = base + (dir ? (G - 1 - c) : c);
       ++t;
       if (r >= n) continue;
       bh = h0 + r % nh;
@@ -326,7 +348,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     // first key tiles land while the current item is still running.
     if (lane == 0 && warp == kQWarp) {
       prefetch_tensormap(&tmQ);
-      Sched sch(n_qp, BH, CAUSAL);
+      Sched<D == 64> sch(n_qp, BH, CAUSAL);
       int bh, qp;
       int nq[2] = {0, 0};  // Q_X copies issued
       bool ok = true;
@@ -353,7 +375,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       const uint32_t full0 = bar(C::B_FULL), empty0 = bar(C::B_EMPTY);
-      Sched sch(n_qp, BH, CAUSAL);
+      Sched<D == 64> sch(n_qp, BH, CAUSAL);
       int bh, qp, n = 0;
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
@@ -393,7 +415,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, BN, false, F16);
       constexpr uint32_t idesc_o = idesc_f32acc(128, C::ON, true, F16);
-      Sched sch(n_qp, BH, CAUSAL);
+      Sched<D == 64> sch(n_qp, BH, CAUSAL);
       int bh, qp;
       // phase bits: P_X tiles (bit x), Q_X items (bit 2 + x), O_X items (bit
       // 4 + x), and "tile X has finished an item" (bit 6 + x)
@@ -536,7 +558,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     // the MMA thread checks no ring barrier in those steps.  It arrives for
     // a phase only after the previous phase has completed.
     if (C::WATCH && lane == 0) {
-      Sched sch(n_qp, BH, CAUSAL);
+      Sched<D == 64> sch(n_qp, BH, CAUSAL);
       RingWalk<C::NUNIT, C::PAIRED> ring;
       int bh, qp;
       uint32_t pa = 0;  // phase parity of "P_A ready"
@@ -574,7 +596,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
     const uint32_t tO = tmem + lane_base + C::TM_O + x * C::O_STRIDE;
     const uint32_t sfull = bar(C::B_SFULL + x), pfull = bar(C::B_PFULL + x);
-    Sched sch(n_qp, BH, CAUSAL);
+    Sched<D == 64> sch(n_qp, BH, CAUSAL);
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
     bool failed = false;
     while (!failed && sch.next(bh, qp)) {
