@@ -171,13 +171,15 @@ struct ItemShape {
 // any shared counter.  Two group shapes:
 //   WIDE = false (D = 128): about two items per CTA per group, the last
 //     group holding whatever heads are left;
-//   WIDE = true (D = 64): about four items per CTA per group, the heads that
+//   WIDE = true (D = 64): about six items per CTA per group, the heads that
 //     would not fill a last group spread over the others (so every group
 //     deals at least G items), and the snake direction carried on from one
 //     group to the next.  On long causal sequences the first shape leaves a
 //     last group of fewer items than CTAs, all of different sizes, and SMs
-//     idle for ~13 % of a launch; at D = 128 the larger groups of the second
-//     shape (twice the K and V in flight) measured slower.
+//     idle for ~13 % of a launch.  A group of about k items per CTA keeps
+//     k * G * 256 * D * 4 bytes of K and V in flight whatever S is: ~60 MB
+//     here, ~40 MB for D = 128 with k = 2, where k = 4 (80 MB) measured
+//     slower.
 template <bool WIDE>
 struct Sched {
   int n_qp, BH, G, c, ng, base_h, extra;
@@ -186,7 +188,7 @@ struct Sched {
   __device__ Sched(int n_qp_, int BH_, bool causal_)
       : n_qp(n_qp_), BH(BH_), G(gridDim.x), c(blockIdx.x), causal(causal_), group(0), t(0),
         rounds(0) {
-    int target = ((WIDE ? 4 : 2) * G + n_qp - 1) / n_qp;  // heads per group
+    int target = ((WIDE ? 6 : 2) * G + n_qp - 1) / n_qp;  // heads per group
     if (target < 1) target = 1;
     if (WIDE) {
       ng = BH / target;
