@@ -46,19 +46,19 @@ TRAFFIC = {
     # profiles/prefill_bf16_d128_causal_b4h32s4096.md
     "prefill": {"kernel": "prefill_bf16", "workload": PREFILL_WORKLOAD,
                 "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "85f9d2688932e0749013dc25bc3349f30752526b94e79dba52dc01cfa4df71a6", "bytes_per_launch": 520967936},
+                "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 521592832},
     # profiles/prefill_bf16_d64_causal_b2h16s16384.md
     "prefill_d64": {"kernel": "prefill_bf16", "workload": "prefill_bf16_b2h16s16384d64",
                     "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "85f9d2688932e0749013dc25bc3349f30752526b94e79dba52dc01cfa4df71a6", "bytes_per_launch": 252809216},
+                    "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 350534656},
     # profiles/prefill_f16_d128_causal_b4h32s4096.md
     "prefill_f16": {"kernel": "prefill_f16", "workload": "prefill_f16_b4h32s4096d128_qk3",
                     "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "85f9d2688932e0749013dc25bc3349f30752526b94e79dba52dc01cfa4df71a6", "bytes_per_launch": 525336064},
+                    "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 526382592},
     # key padding, B4 H32 S4096 D128 (one capture of the same bench command, dram metrics only)
     "prefill_varlen": {"kernel": "prefill_bf16", "workload": "prefill_varlen_bf16_b4h32s4096d128",
                        "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                       "sha256": "85f9d2688932e0749013dc25bc3349f30752526b94e79dba52dc01cfa4df71a6", "bytes_per_launch": 458075904},
+                       "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 462195968},
     # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
     "decode": {"kernel": "decode", "workload": DECODE_WORKLOAD, "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1201886720},
