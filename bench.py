@@ -41,24 +41,27 @@ DECODE_WORKLOAD = "decode_bf16_b16h32d128_len512_8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
-# named workload, valid only while the kernel source hashes to the recorded value.
+# named workload, valid only while the kernel source hashes to the recorded value.  The prefill
+# records come from one-pass captures (those metrics only) of `bench.py --only prefill
+# --prefill-workload <workload> --steps 1 --warmup 1 --profile`; the profiles named beside
+# them hold the full captures of the same kernels.
 TRAFFIC = {
     # profiles/prefill_bf16_d128_causal_b4h32s4096.md
     "prefill": {"kernel": "prefill_bf16", "workload": PREFILL_WORKLOAD,
                 "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 521592832},
+                "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 519273728},
     # profiles/prefill_bf16_d64_causal_b2h16s16384.md
     "prefill_d64": {"kernel": "prefill_bf16", "workload": "prefill_bf16_b2h16s16384d64",
                     "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 350534656},
+                    "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 345352960},
     # profiles/prefill_f16_d128_causal_b4h32s4096.md
     "prefill_f16": {"kernel": "prefill_f16", "workload": "prefill_f16_b4h32s4096d128_qk3",
                     "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 526382592},
+                    "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 522228992},
     # key padding, B4 H32 S4096 D128 (one capture of the same bench command, dram metrics only)
     "prefill_varlen": {"kernel": "prefill_bf16", "workload": "prefill_varlen_bf16_b4h32s4096d128",
                        "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                       "sha256": "f33b3c3f206cbc046a034ab31ce8fa804e841599a8fe62a66b12d8b8971ac849", "bytes_per_launch": 462195968},
+                       "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 453030656},
     # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
     "decode": {"kernel": "decode", "workload": DECODE_WORKLOAD, "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1201886720},
@@ -66,13 +69,17 @@ TRAFFIC = {
     "decode_f16": {"kernel": "decode", "workload": "decode_f16_b16h32d128_len512_8192",
                    "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
                    "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1292623616},
-    # profiles/proj_gemm_bf16_b4s4096_h32d128.md (both projection kernels, one capture)
+    # profiles/proj_gemm_bf16_b4s4096_h32d128.md (the projection kernels; these figures from one
+    # one-pass DRAM capture of `bench.py --only projections --steps 1 --warmup 1 --profile`)
     "qkv_proj": {"kernel": "qkv_proj", "workload": "qkv_bf16_b4s4096hid4096_h32d128",
                  "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                 "sha256": "9d394e353523791f3121bbbb7638f1a7c6dd93b822b862823ba7f5de988572dc", "bytes_per_launch": 1352056576},
+                 "sha256": "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", "bytes_per_launch": 1354212608},
+    "out_proj_rows": {"kernel": "out_proj_rows", "workload": "outproj_bf16_b4h32s4096d128_n4096",
+                      "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
+                      "sha256": "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", "bytes_per_launch": 396940544},
     "out_proj": {"kernel": "out_proj", "workload": "outproj_bf16_b4h32s4096d128_n4096",
                  "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                 "sha256": "9d394e353523791f3121bbbb7638f1a7c6dd93b822b862823ba7f5de988572dc", "bytes_per_launch": 409215744},
+                 "sha256": "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", "bytes_per_launch": 404913152},
 }
 
 
@@ -569,6 +576,7 @@ def run_projections(args, rank, world, dist):
     shp = (xq.B, xq.H, xq.S, xq.D)
     Q, K, V = (torch.empty(shp, dtype=torch.bfloat16, device=dev) for _ in range(3))
     O, Wo = dev16(xo.O), dev16(xo.W)
+    O_rows = O.permute(0, 2, 1, 3).contiguous()  # the same O as [B, S, H, D]
     Y = torch.empty((xo.B, xo.S, xo.n_out), dtype=torch.bfloat16, device=dev)
     M = xq.B * xq.S
     f_qkv = 2.0 * M * xq.hidden * 3 * xq.H * xq.D
@@ -580,6 +588,8 @@ def run_projections(args, rank, world, dist):
         ev[1].record(stream)
         mha.mha_out_proj(O, Wo, Y=Y, stream=stream)
         ev[2].record(stream)
+        mha.mha_out_proj(O_rows, Wo, Y=Y, stream=stream, o_layout="bshd")
+        ev[3].record(stream)
 
     def barrier():
         if dist is not None:
@@ -587,11 +597,11 @@ def run_projections(args, rank, world, dist):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     barrier()
     if mha.mha_get_device_status(stream) != 0:
         raise RuntimeError("device status after warm-up")
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clock = ClockSampler(local)
     if not args.profile:
         clock.start()
@@ -608,8 +618,9 @@ def run_projections(args, rank, world, dist):
         raise RuntimeError("device status after timed region")
     tq = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
     to = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    tr = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3
     total = t0.elapsed_time(t1) / 1e3
-    tq, to, total = max_over_ranks([tq, to, total], dist, dev)
+    tq, to, tr, total = max_over_ranks([tq, to, tr, total], dist, dev)
     if rank != 0:
         return 0
     K_ = args.steps
@@ -637,7 +648,10 @@ def run_projections(args, rank, world, dist):
             "roofline": roof("qkv_proj_kernel", f_qkv, tq, 0, traffic_for("qkv_proj", QKV_WORKLOAD)),
             "out_proj": roof("out_proj_kernel", f_out, to, 1,
                              traffic_for("out_proj", OUTPROJ_WORKLOAD)),
-            "clocks": clocks, "gpu_launches": 2 * K_}
+            # the same product with O already in [B, S, H, D] (mha_fwd_ex o_layout 1)
+            "out_proj_rows": roof("out_proj_rows_kernel", f_out, tr, 2,
+                                  traffic_for("out_proj_rows", OUTPROJ_WORKLOAD)),
+            "clocks": clocks, "gpu_launches": 3 * K_}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -61,6 +61,10 @@ def _declare(lib):
     lib.mha_qkv_proj.restype = i
     lib.mha_out_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
     lib.mha_out_proj.restype = i
+    lib.mha_out_proj_ex.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.mha_out_proj_ex.restype = i
+    lib.mha_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+    lib.mha_fwd_ex.restype = i
     lib.mha_decode_num_splits.argtypes = [i, i]
     lib.mha_decode_num_splits.restype = i
     lib.mha_get_device_status.argtypes = [vp]
@@ -167,6 +171,45 @@ def mha_fwd_varlen_f16(Q, K, V, key_lens, O=None, LSE=None, scale=None, causal=T
                     want_lse, key_lens=key_lens)
 
 
+def mha_fwd_ex(Q, K, V, key_lens=None, O=None, LSE=None, scale=None, causal=True,
+               o_layout="bhsd", stream=None, want_lse=True):
+    """bf16 or f16 prefill (from Q's dtype), optional key padding, and O either
+    [B, H, S, D] (o_layout "bhsd") or [B, S, H, D] ("bshd", the concatenated
+    heads an output projection reads as rows).  Returns (O, LSE).  See
+    include/mha.h: mha_fwd_ex."""
+    if Q.dim() != 4:
+        raise ValueError("Q must be [B, H, S, D]")
+    if Q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("Q must be bf16 or f16")
+    if o_layout not in ("bhsd", "bshd"):
+        raise ValueError("o_layout must be 'bhsd' or 'bshd'")
+    B, H, S, D = Q.shape
+    dev = Q.device
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _check(t, name, Q.dtype, (B, H, S, D), dev)
+    oshape = (B, H, S, D) if o_layout == "bhsd" else (B, S, H, D)
+    if O is None:
+        O = torch.empty(oshape, dtype=Q.dtype, device=dev)
+    _check(O, "O", Q.dtype, oshape, dev)
+    if LSE is None and want_lse:
+        LSE = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    if LSE is not None:
+        _check(LSE, "LSE", torch.float32, (B, H, S), dev)
+    if key_lens is not None:
+        _check(key_lens, "key_lens", torch.int32, (B,), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = _load().mha_fwd_ex(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                            LSE.data_ptr() if LSE is not None else None,
+                            key_lens.data_ptr() if key_lens is not None else None,
+                            B, H, S, D, float(scale), int(bool(causal)),
+                            1 if Q.dtype == torch.float16 else 0,
+                            0 if o_layout == "bhsd" else 1, _stream_ptr(stream, dev))
+    if st != MHA_OK:
+        raise MHAError(st, "mha_fwd_ex")
+    return O, LSE
+
+
 def mha_fwd_f32(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None, want_lse=True):
     """float32 [B,H,S,D] prefill; returns (O, LSE).  See include/mha.h: mha_fwd_f32."""
     return _prefill("mha_fwd_f32", torch.float32, Q, K, V, O, LSE, scale, causal, stream,
@@ -262,14 +305,20 @@ def mha_qkv_proj(X, W, H: int, D: int, Q=None, K=None, V=None, stream=None):
     return tuple(out)
 
 
-def mha_out_proj(O, W, Y=None, stream=None):
-    """Output projection Y = concat_h(O_h) W_O, bf16; O [B, H, S, D], W [H*D, n_out];
-    returns Y [B, S, n_out].  See include/mha.h: mha_out_proj."""
+def mha_out_proj(O, W, Y=None, stream=None, o_layout="bhsd"):
+    """Output projection Y = concat_h(O_h) W_O, bf16; O [B, H, S, D] (o_layout
+    "bhsd") or [B, S, H, D] ("bshd"), W [H*D, n_out]; returns Y [B, S, n_out].
+    See include/mha.h: mha_out_proj, mha_out_proj_ex."""
     if O.dim() != 4:
-        raise ValueError("O must be [B, H, S, D]")
-    B, H, S, D = O.shape
+        raise ValueError("O must be 4-D")
+    if o_layout == "bhsd":
+        B, H, S, D = O.shape
+    elif o_layout == "bshd":
+        B, S, H, D = O.shape
+    else:
+        raise ValueError("o_layout must be 'bhsd' or 'bshd'")
     dev = O.device
-    _check(O, "O", torch.bfloat16, (B, H, S, D), dev)
+    _check(O, "O", torch.bfloat16, tuple(O.shape), dev)
     if W.dim() != 2 or W.shape[0] != H * D:
         raise ValueError("W must be [H*D, n_out]")
     n_out = W.shape[1]
@@ -277,8 +326,8 @@ def mha_out_proj(O, W, Y=None, stream=None):
     if Y is None:
         Y = torch.empty((B, S, n_out), dtype=torch.bfloat16, device=dev)
     _check(Y, "Y", torch.bfloat16, (B, S, n_out), dev)
-    st = _load().mha_out_proj(O.data_ptr(), W.data_ptr(), Y.data_ptr(), B, H, S, D, n_out,
-                              _stream_ptr(stream, dev))
+    st = _load().mha_out_proj_ex(O.data_ptr(), W.data_ptr(), Y.data_ptr(), B, H, S, D, n_out,
+                                 0 if o_layout == "bhsd" else 1, _stream_ptr(stream, dev))
     if st != MHA_OK:
         raise MHAError(st, "mha_out_proj")
     return Y

@@ -14,7 +14,8 @@
 // - Output projection: the same page's section 2.1 lists it after attention
 //   as one more GEMM, Y = concat_h(O_h) W_O; A is read from O [B, H, S, D]
 //   through a 4-D view (d, s, h, b), so row (b, s) and column h*D + d of the
-//   concatenation come from O without a transpose.
+//   concatenation come from O without a transpose -- or, when attention wrote
+//   O as [B, S, H, D], as the plain row-major [B*S][H*D] matrix it then is.
 //
 // Each output tile of 256 rows x 256 columns belongs to a pair of CTAs (a
 // cluster of 2 on two SMs): one thread of the even CTA issues
@@ -179,7 +180,12 @@ struct TileMap {
   }
 };
 
-template <bool OUT>
+// MODE: the Q/K/V projection (A = X as [M][Kd], epilogue into Q, K, V),
+// the output projection with A = O [B, H, S, D] through its 4-D view, or the
+// output projection with A = O [B, S, H, D] read as rows [B*S][H*D].
+enum : int { MODE_QKV = 0, MODE_OUT_BHSD = 1, MODE_OUT_ROWS = 2 };
+
+template <int MODE>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmW,
                                           uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko,
                                           uint16_t* __restrict__ Vo, int tiles_m, int M, int N,
@@ -247,7 +253,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const uint32_t full = full_leader + 8u * st;
           // the leader's barrier counts both CTAs' bytes of this stage
           if (leader) mbar_arrive_expect_tx(bar(B_FULL + st), 2 * STAGE_BYTES);
-          if constexpr (OUT) {
+          if constexpr (MODE == MODE_OUT_BHSD) {
             const int b = mt / sblocks, sb = mt - b * sblocks, k0 = kb * GK;
             tma2_load_4d(dst, &tmA, full, k0 % D, sb * 2 * GM + static_cast<int>(rank) * GM,
                          k0 / D, b);
@@ -328,10 +334,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       tmap.get(t, mt, nt);
       int b, s;
       bool row_ok;
-      if constexpr (OUT) {
+      if constexpr (MODE == MODE_OUT_BHSD) {
         b = mt / sblocks;
         s = (mt - b * sblocks) * 2 * GM + static_cast<int>(rank) * GM + r;
         row_ok = s < S;
+      } else if constexpr (MODE == MODE_OUT_ROWS) {
+        b = 0;  // row m of Y is row m of A
+        s = mt * 2 * GM + static_cast<int>(rank) * GM + r;
+        row_ok = s < M;
       } else {
         const int m = mt * 2 * GM + static_cast<int>(rank) * GM + r;
         row_ok = m < M;
@@ -345,8 +355,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         const int n0 = nt * GN + c * 32;
         if (row_ok && n0 < N) {
           uint16_t* dst;
-          if constexpr (OUT) {
+          if constexpr (MODE == MODE_OUT_BHSD) {
             dst = Qo + (static_cast<size_t>(b) * S + s) * N + n0;
+          } else if constexpr (MODE == MODE_OUT_ROWS) {
+            dst = Qo + static_cast<size_t>(s) * N + n0;
           } else {
             const int which = n0 / HD, rem = n0 - which * HD;
             const int h = rem / D, d0 = rem - h * D;
@@ -379,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
                     int M, int N, int Kd, int S, int H, int D, uint64_t wait_limit_ns) {
-  gemm_body<false>(tmX, tmW, Qo, Ko, Vo, (M + 2 * GM - 1) / (2 * GM), M, N, Kd, S, H, D, 0,
+  gemm_body<MODE_QKV>(tmX, tmW, Qo, Ko, Vo, (M + 2 * GM - 1) / (2 * GM), M, N, Kd, S, H, D, 0,
                    wait_limit_ns);
 }
 
@@ -388,8 +400,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint16_t* __restrict__ Y, int B, int N, int Kd, int S, int D,
                     uint64_t wait_limit_ns) {
   const int sblocks = (S + 2 * GM - 1) / (2 * GM);
-  gemm_body<true>(tmO, tmW, Y, nullptr, nullptr, B * sblocks, 0, N, Kd, S, 0, D, sblocks,
-                  wait_limit_ns);
+  gemm_body<MODE_OUT_BHSD>(tmO, tmW, Y, nullptr, nullptr, B * sblocks, 0, N, Kd, S, 0, D,
+                           sblocks, wait_limit_ns);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    out_proj_rows_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmW, uint16_t* __restrict__ Y, int M,
+                         int N, int Kd, uint64_t wait_limit_ns) {
+  gemm_body<MODE_OUT_ROWS>(tmA, tmW, Y, nullptr, nullptr, (M + 2 * GM - 1) / (2 * GM), M, N, Kd,
+                           1, 0, 64, 0, wait_limit_ns);
 }
 
 // ---------------------------------------------------------------- host side
@@ -475,18 +495,30 @@ cudaError_t launch_pairs(Kern kern, long long pair_tiles, cudaStream_t stream,
 }  // namespace
 
 cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D,
-                            int n_out, cudaStream_t stream, uint64_t wait_limit_ns) {
+                            int n_out, int o_layout, cudaStream_t stream, uint64_t wait_limit_ns) {
   const int Kd = H * D, N = n_out;
   CUtensorMap mo, mw;
-  if (!encode_bhsd_4d(&mo, O, B, H, S, D) || !encode_2d(&mw, W, Kd, N, 64, GK))
-    return cudaErrorInvalidValue;
-  const long long tiles = static_cast<long long>(B) * ((S + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
+  if (!encode_2d(&mw, W, Kd, N, 64, GK)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr = {};
-  cudaError_t e = launch_pairs(out_proj_kernel, tiles, stream, cfg, attr);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   uint16_t* y = static_cast<uint16_t*>(Y);
-  e = cudaLaunchKernelEx(&cfg, out_proj_kernel, mo, mw, y, B, N, Kd, S, D, wait_limit_ns);
+  if (o_layout == 1) {
+    // O [B, S, H, D] is the row-major [B*S][H*D] matrix of concatenated heads
+    const int M = B * S;
+    if (!encode_2d(&mo, O, M, Kd, GK, GM)) return cudaErrorInvalidValue;
+    const long long tiles = static_cast<long long>((M + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
+    e = launch_pairs(out_proj_rows_kernel, tiles, stream, cfg, attr);
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, out_proj_rows_kernel, mo, mw, y, M, N, Kd, wait_limit_ns);
+  } else {
+    if (!encode_bhsd_4d(&mo, O, B, H, S, D)) return cudaErrorInvalidValue;
+    const long long tiles =
+        static_cast<long long>(B) * ((S + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
+    e = launch_pairs(out_proj_kernel, tiles, stream, cfg, attr);
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, out_proj_kernel, mo, mw, y, B, N, Kd, S, D, wait_limit_ns);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

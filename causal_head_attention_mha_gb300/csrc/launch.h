@@ -11,16 +11,17 @@ constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 // key_lens: device int32 [B] of valid key counts (key padding), or nullptr.
+// o_layout: 0 = O as [B, H, S, D], 1 = O as [B, S, H, D].
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 const int* key_lens, int B, int H, int S, int D, float scale,
-                                int causal, cudaStream_t stream, uint64_t wait_limit_ns,
-                                int inject);
+                                int causal, int o_layout, cudaStream_t stream,
+                                uint64_t wait_limit_ns, int inject);
 
 // The same on f16 inputs and outputs (P rounded to f16).
 cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                const int* key_lens, int B, int H, int S, int D, float scale,
-                               int causal, cudaStream_t stream, uint64_t wait_limit_ns,
-                               int inject);
+                               int causal, int o_layout, cudaStream_t stream,
+                               uint64_t wait_limit_ns, int inject);
 
 cudaError_t launch_prefill_f32(const float* Q, const float* K, const float* V, float* O,
                                float* LSE, int B, int H, int S, int D, float scale, int causal,
@@ -43,8 +44,9 @@ cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void
 
 // Output projection Y = concat_h(O_h) W_O: O [B, H, S, D], W [H*D][n_out] row-major,
 // Y [B, S, n_out] row-major, bf16.
+// o_layout: 0 = O read as [B, H, S, D], 1 = O read as [B, S, H, D] (row-major A).
 cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D,
-                            int n_out, cudaStream_t stream, uint64_t wait_limit_ns);
+                            int n_out, int o_layout, cudaStream_t stream, uint64_t wait_limit_ns);
 
 // Read and clear the device error word of the prefill / projection translation unit.
 cudaError_t take_prefill_bf16_error(unsigned int* word);

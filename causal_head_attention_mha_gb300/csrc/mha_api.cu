@@ -64,7 +64,7 @@ int mha_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, in
   const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
   if (st != MHA_OK) return st;
   const cudaError_t e =
-      mha::launch_prefill_bf16(Q, K, V, O, LSE, nullptr, B, H, S, D, scale, causal,
+      mha::launch_prefill_bf16(Q, K, V, O, LSE, nullptr, B, H, S, D, scale, causal, 0,
                                static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
                                g_fault_injection.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
@@ -75,7 +75,7 @@ int mha_fwd_f16(const void* Q, const void* K, const void* V, void* O, float* LSE
   const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
   if (st != MHA_OK) return st;
   const cudaError_t e =
-      mha::launch_prefill_f16(Q, K, V, O, LSE, nullptr, B, H, S, D, scale, causal,
+      mha::launch_prefill_f16(Q, K, V, O, LSE, nullptr, B, H, S, D, scale, causal, 0,
                               static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
                               g_fault_injection.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
@@ -89,7 +89,7 @@ int mha_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* 
   if (!key_lens) return MHA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(key_lens) & 3u) return MHA_ERR_MISALIGNED;
   const cudaError_t e =
-      mha::launch_prefill_bf16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal,
+      mha::launch_prefill_bf16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, 0,
                                static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
                                g_fault_injection.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
@@ -103,9 +103,27 @@ int mha_fwd_varlen_f16(const void* Q, const void* K, const void* V, void* O, flo
   if (!key_lens) return MHA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(key_lens) & 3u) return MHA_ERR_MISALIGNED;
   const cudaError_t e =
-      mha::launch_prefill_f16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal,
+      mha::launch_prefill_f16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, 0,
                               static_cast<cudaStream_t>(stream), g_wait_limit_ns.load(),
                               g_fault_injection.load());
+  return e == cudaSuccess ? MHA_OK : cuda_fail(e);
+}
+
+int mha_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               const int* key_lens, int B, int H, int S, int D, float scale, int causal,
+               int dtype, int o_layout, void* stream) {
+  const int st = check_prefill(Q, K, V, O, LSE, B, H, S, D, scale, causal);
+  if (st != MHA_OK) return st;
+  if ((dtype != 0 && dtype != 1) || (o_layout != 0 && o_layout != 1)) return MHA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(key_lens) & 3u) return MHA_ERR_MISALIGNED;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      dtype == 1 ? mha::launch_prefill_f16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal,
+                                           o_layout, s, g_wait_limit_ns.load(),
+                                           g_fault_injection.load())
+                 : mha::launch_prefill_bf16(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal,
+                                            o_layout, s, g_wait_limit_ns.load(),
+                                            g_fault_injection.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);
 }
 
@@ -185,6 +203,11 @@ int mha_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B,
 
 int mha_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D, int n_out,
                  void* stream) {
+  return mha_out_proj_ex(O, W, Y, B, H, S, D, n_out, 0, stream);
+}
+
+int mha_out_proj_ex(const void* O, const void* W, void* Y, int B, int H, int S, int D, int n_out,
+                    int o_layout, void* stream) {
   if (!O || !W || !Y) return MHA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1 || D < 1 || n_out < 1) return MHA_ERR_INVALID_ARG;
   const long long M = static_cast<long long>(B) * S, Kd = static_cast<long long>(H) * D;
@@ -192,8 +215,9 @@ int mha_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int
     return MHA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return MHA_ERR_UNSUPPORTED;
   if (n_out % 32 != 0) return MHA_ERR_UNSUPPORTED;  // 32-column store chunks
+  if (o_layout != 0 && o_layout != 1) return MHA_ERR_UNSUPPORTED;
   if (!aligned16(O) || !aligned16(W) || !aligned16(Y)) return MHA_ERR_MISALIGNED;
-  const cudaError_t e = mha::launch_out_proj(O, W, Y, B, H, S, D, n_out,
+  const cudaError_t e = mha::launch_out_proj(O, W, Y, B, H, S, D, n_out, o_layout,
                                              static_cast<cudaStream_t>(stream),
                                              g_wait_limit_ns.load());
   return e == cudaSuccess ? MHA_OK : cuda_fail(e);

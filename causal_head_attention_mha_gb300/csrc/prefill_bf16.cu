@@ -274,11 +274,20 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
                                              const CUtensorMap& tmV, uint16_t* __restrict__ O,
                                              float* __restrict__ lse, int S, int BH, float c_log2,
                                              const int* __restrict__ key_lens, int H,
-                                             uint64_t wait_limit_ns, int inject) {
+                                             int o_bshd, uint64_t wait_limit_ns, int inject) {
   using C = Cfg<D>;
   using E = Elem<F16>;
   // valid keys of the sequence of (b, h) = bh: key_lens[b] clamped to [0, S]
   // with key padding (VARLEN), else S
+  // element offset of row (bh, q) of O: [B, H, S, D], or [B, S, H, D] when
+  // o_bshd (the concatenated-heads layout an output projection reads as rows)
+  auto o_row = [&](int bh, int q) -> size_t {
+    if (o_bshd) {
+      const int b = bh / H, h = bh - b * H;
+      return ((static_cast<size_t>(b) * S + q) * H + h) * D;
+    }
+    return (static_cast<size_t>(bh) * S + q) * D;
+  };
   auto key_len = [&](int bh) {
     if constexpr (VARLEN) return min(max(__ldg(key_lens + bh / H), 0), S);
     (void)bh;
@@ -610,7 +619,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
         // a sequence without any valid key (L = 0): its rows are the empty
         // sum, O = 0 and LSE = -inf
         if (VARLEN && (x == 0 || sh.hasB) && q < S) {
-          uint16_t* orow = O + (static_cast<size_t>(bh) * S + q) * D;
+          uint16_t* orow = O + o_row(bh, q);
 #pragma unroll
           for (int c = 0; c < D; c += 8) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
           if (lse != nullptr) lse[static_cast<size_t>(bh) * S + q] = -INFINITY;
@@ -752,7 +761,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
         lp = __uint_as_float(t[0]);
       }
       const float inv_lp = 1.0f / lp;
-      uint16_t* orow = O + (static_cast<size_t>(bh) * S + q) * D;
+      uint16_t* orow = O + o_row(bh, q);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -791,9 +800,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       NAME(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, \
            const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,                \
            float* __restrict__ lse, int S, int BH, float c_log2,                             \
-           const int* __restrict__ key_lens, int H, uint64_t wait_limit_ns, int inject) {    \
+           const int* __restrict__ key_lens, int H, int o_bshd, uint64_t wait_limit_ns,      \
+           int inject) {                                                                     \
     prefill_body<D, CAUSAL, F16, VARLEN>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H,  \
-                                         wait_limit_ns, inject);                            \
+                                         o_bshd, wait_limit_ns, inject);                    \
   }
 MHA_PREFILL_KERNEL(prefill_bf16_kernel, false, false)
 MHA_PREFILL_KERNEL(prefill_f16_kernel, true, false)
@@ -840,7 +850,8 @@ bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D, bool f
 template <int D, bool CAUSAL, bool F16, bool VARLEN>
 cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                      uint16_t* O, float* lse, int BH, int S, float c_log2, const int* key_lens,
-                     int H, cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
+                     int H, int o_bshd, cudaStream_t stream, uint64_t wait_limit_ns,
+                     int inject) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
   auto kern = VARLEN ? (F16 ? prefill_f16_varlen_kernel<D, CAUSAL> : prefill_bf16_varlen_kernel<D, CAUSAL>)
                      : (F16 ? prefill_f16_kernel<D, CAUSAL> : prefill_bf16_kernel<D, CAUSAL>);
@@ -858,7 +869,7 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   const int nsm = device_sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
   const unsigned grid = static_cast<unsigned>(items < nsm ? items : nsm);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, O, lse, S, BH, c_log2, key_lens, H,
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, O, lse, S, BH, c_log2, key_lens, H, o_bshd,
                                          wait_limit_ns, inject);
   return cudaGetLastError();
 }
@@ -866,7 +877,8 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 template <bool F16>
 cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O, float* LSE,
                            const int* key_lens, int B, int H, int S, int D, float scale,
-                           int causal, cudaStream_t stream, uint64_t wait_limit_ns, int inject) {
+                           int causal, int o_layout, cudaStream_t stream, uint64_t wait_limit_ns,
+                           int inject) {
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   if (!encode_bhsd(&mq, Q, BH, S, D, F16) || !encode_bhsd(&mk, K, BH, S, D, F16) ||
@@ -875,7 +887,8 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
   const float c_log2 = scale * 1.44269504088896340736f;  // scale * log2(e)
   uint16_t* o = static_cast<uint16_t*>(O);
 #define MHA_LAUNCH(DD, CC, VL) \
-  launch_t<DD, CC, F16, VL>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, stream, wait_limit_ns, inject)
+  launch_t<DD, CC, F16, VL>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, o_layout, stream, \
+                            wait_limit_ns, inject)
   if (key_lens != nullptr) {
     if (D == 128) return causal ? MHA_LAUNCH(128, true, true) : MHA_LAUNCH(128, false, true);
     return causal ? MHA_LAUNCH(64, true, true) : MHA_LAUNCH(64, false, true);
@@ -889,18 +902,18 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
 
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 const int* key_lens, int B, int H, int S, int D, float scale,
-                                int causal, cudaStream_t stream, uint64_t wait_limit_ns,
-                                int inject) {
-  return launch_prefill<false>(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, stream,
-                               wait_limit_ns, inject);
+                                int causal, int o_layout, cudaStream_t stream,
+                                uint64_t wait_limit_ns, int inject) {
+  return launch_prefill<false>(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, o_layout,
+                               stream, wait_limit_ns, inject);
 }
 
 cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                const int* key_lens, int B, int H, int S, int D, float scale,
-                               int causal, cudaStream_t stream, uint64_t wait_limit_ns,
-                               int inject) {
-  return launch_prefill<true>(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, stream,
-                              wait_limit_ns, inject);
+                               int causal, int o_layout, cudaStream_t stream,
+                               uint64_t wait_limit_ns, int inject) {
+  return launch_prefill<true>(Q, K, V, O, LSE, key_lens, B, H, S, D, scale, causal, o_layout,
+                              stream, wait_limit_ns, inject);
 }
 
 cudaError_t take_prefill_bf16_error(unsigned int* word) {

@@ -213,6 +213,35 @@ int mha_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int
                  void* stream);
 
 /*
+ * The prefill of mha_fwd / mha_fwd_f16 / mha_fwd_varlen(_f16) behind one
+ * entry point, with a choice of O's layout.
+ *
+ *   dtype    : 0 = bf16, 1 = f16 (Q, K, V and O).
+ *   key_lens : as in mha_fwd_varlen, or NULL for no key padding.
+ *   o_layout : 0 = O as [B, H, S, D] (as mha_fwd);
+ *              1 = O as [B, S, H, D]: row (b, s) holds the heads of position s
+ *              side by side (feature h*D + d), the concatenation the output
+ *              projection multiplies by W_O (page "Week 4 CUDA notes"
+ *              section 2.1), so that product reads O as a plain row-major
+ *              [B*S, H*D] matrix (mha_out_proj_ex with o_layout 1).
+ *   Q, K, V, LSE, sizes, scale, causal and errors as mha_fwd; an unknown
+ *   dtype or o_layout returns MHA_ERR_UNSUPPORTED.
+ */
+int mha_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               const int* key_lens, int B, int H, int S, int D, float scale, int causal,
+               int dtype, int o_layout, void* stream);
+
+/*
+ * mha_out_proj with a choice of O's layout: o_layout 0 reads O as
+ * [B, H, S, D] (as mha_out_proj), 1 reads O as [B, S, H, D], the row-major
+ * [B*S, H*D] matrix of concatenated heads (what mha_fwd_ex writes with
+ * o_layout 1).  Y, W, sizes and errors as mha_out_proj; the sums are taken in
+ * the same order either way, so both layouts give the same Y bit for bit.
+ */
+int mha_out_proj_ex(const void* O, const void* W, void* Y, int B, int H, int S, int D, int n_out,
+                    int o_layout, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * bounded waits set.  Returns MHA_OK, MHA_ERR_TIMEOUT when a wait in some
  * kernel of this library ran out since the last call, or MHA_ERR_CUDA when

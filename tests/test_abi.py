@@ -158,3 +158,28 @@ def test_out_proj_validation(lib, kw, expected):
     a.update(kw)
     assert lib.mha_out_proj(a["O"], a["W"], a["Y"], a["B"], a["H"], a["S"], a["D"], a["n_out"],
                             None) == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(Q=None), INVALID), (dict(B=0), INVALID), (dict(D=96), UNSUPPORTED),
+    (dict(dtype=2), UNSUPPORTED), (dict(o_layout=2), UNSUPPORTED), (dict(o_layout=-1), UNSUPPORTED),
+    (dict(key_lens=FAKE + 2), MISALIGNED), (dict(O=FAKE + 8), MISALIGNED),
+])
+def test_fwd_ex_validation(lib, kw, expected):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, LSE=None, key_lens=None, B=1, H=2, S=128, D=64,
+             scale=0.125, causal=1, dtype=0, o_layout=1)
+    a.update(kw)
+    assert lib.mha_fwd_ex(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["key_lens"], a["B"], a["H"],
+                          a["S"], a["D"], a["scale"], a["causal"], a["dtype"], a["o_layout"],
+                          None) == expected
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(O=None), INVALID), (dict(o_layout=2), UNSUPPORTED), (dict(n_out=48), UNSUPPORTED),
+    (dict(W=FAKE + 8), MISALIGNED),
+])
+def test_out_proj_ex_validation(lib, kw, expected):
+    a = dict(O=FAKE, W=FAKE, Y=FAKE, B=1, H=2, S=128, D=64, n_out=256, o_layout=1)
+    a.update(kw)
+    assert lib.mha_out_proj_ex(a["O"], a["W"], a["Y"], a["B"], a["H"], a["S"], a["D"], a["n_out"],
+                               a["o_layout"], None) == expected
