@@ -1,6 +1,8 @@
-"""The FMA-pipe exp2 of the prefill kernel, emulated in fp32 on the CPU.
+"""The FMA-pipe exp2 kept in csrc/ptx.cuh (exp2_poly2), emulated in fp32 on the CPU.
 
-The kernel computes 2^x as 2^round(x) * p(x - round(x)) with the minimax
+No kernel calls it today: handing part of the exponentials to the FMA pipe
+measured slower than the special-function unit alone on this GPU.  It
+computes 2^x as 2^round(x) * p(x - round(x)) with the minimax
 polynomial of csrc/exp2_poly.h (written by csrc/gen_exp2_poly.py from the
 Remez exchange algorithm).  This test re-evaluates that sequence in float32
 (products and sums rounded to float32 as the fused multiply-adds would be,
