@@ -57,6 +57,8 @@ def _declare(lib):
     lib.mha_decode_f16.restype = i
     lib.mha_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
     lib.mha_decode_noalloc.restype = i
+    lib.mha_decode_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, i, i, vp]
+    lib.mha_decode_ex.restype = i
     lib.mha_qkv_proj.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.mha_qkv_proj.restype = i
     lib.mha_out_proj.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
@@ -216,7 +218,7 @@ def mha_fwd_f32(Q, K, V, O=None, LSE=None, scale=None, causal=True, stream=None,
                     want_lse)
 
 
-def _decode(entry, dtype, q, Kcache, Vcache, seqlens, O, scale, stream):
+def _decode(entry, dtype, q, Kcache, Vcache, seqlens, O, scale, stream, extra=()):
     if q.dim() != 3:
         raise ValueError("q must be [B, H, D]")
     B, H, D = q.shape
@@ -234,7 +236,7 @@ def _decode(entry, dtype, q, Kcache, Vcache, seqlens, O, scale, stream):
         scale = 1.0 / math.sqrt(D)
     st = getattr(_load(), entry)(q.data_ptr(), Kcache.data_ptr(), Vcache.data_ptr(),
                                  seqlens.data_ptr(), O.data_ptr(), B, H, D, float(scale),
-                                 _stream_ptr(stream, dev))
+                                 *extra, _stream_ptr(stream, dev))
     if st != MHA_OK:
         raise MHAError(st, entry)
     return O
@@ -251,6 +253,17 @@ def mha_decode(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
 def mha_decode_f16(q, Kcache, Vcache, seqlens, O=None, scale=None, stream=None):
     """mha_decode on f16 q, cache and O.  See include/mha.h: mha_decode_f16."""
     return _decode("mha_decode_f16", torch.float16, q, Kcache, Vcache, seqlens, O, scale, stream)
+
+
+def mha_decode_ex(q, Kcache, Vcache, seqlens, O=None, scale=None, nsplit=0, stream=None):
+    """mha_decode / mha_decode_f16 (by q's dtype) with the number of key splits
+    chosen by the caller: 0 = automatic, 1..64 = that many.  See include/mha.h:
+    mha_decode_ex."""
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("q must be bf16 or f16")
+    dtype_code = 1 if q.dtype == torch.float16 else 0
+    return _decode("mha_decode_ex", q.dtype, q, Kcache, Vcache, seqlens, O, scale, stream,
+                   extra=(int(nsplit), dtype_code))
 
 
 def mha_decode_noalloc(q, Kcache, Vcache, seqlens, O, scale=None, stream=None):

@@ -277,7 +277,7 @@ int decode_num_splits(int B, int H, int num_sms) {
   const long long rows = static_cast<long long>(B) * H;
   long long n = (16LL * num_sms + rows - 1) / rows;
   if (n < 1) n = 1;
-  if (n > 64) n = 64;
+  if (n > kMaxDecodeSplits) n = kMaxDecodeSplits;
   return static_cast<int>(n);
 }
 

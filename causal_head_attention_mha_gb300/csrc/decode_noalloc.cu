@@ -12,6 +12,7 @@
 // every device that loads the library until the process exits.
 #include <cstdint>
 #include <mutex>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mha.h"
@@ -26,25 +27,73 @@ static_assert(MHA_DECODE_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size must be
 // stand-in symbol.  The device address is looked up per device below.
 static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
 
+// The array's address belongs to the module as loaded into one CUDA context.
+// A context that is destroyed and created again (cudaDeviceReset, or a
+// primary context released and retained) loads the module again, possibly
+// elsewhere, so a remembered address is only reused while the current
+// context is the one it was looked up in: the cache is keyed on the
+// context's unique ID (cuCtxGetId), which a new context never repeats.
 constexpr int kMaxDevices = 64;
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;  // 0: nothing looked up yet
+  float* ptr = nullptr;
+};
 std::mutex g_setup_mutex;
-float* g_scratch_on_device[kMaxDevices] = {};
+ScratchSlot g_scratch_on_device[kMaxDevices];
 
-// Device address of g_decode_scratch on the current device; looked up once
-// per device (with that device current) and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique ID of the calling thread's current context, or 0 when no context
+// is current yet.
+cudaError_t current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  *id = 0;
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+// Device address of g_decode_scratch in the current context; looked up once
+// per context (with its device current) and cached.
 cudaError_t scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long ctx_id = 0;
+  e = current_context_id(&ctx_id);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_on_device[dev] == nullptr) {
+  ScratchSlot& slot = g_scratch_on_device[dev];
+  if (ctx_id == 0 || slot.ctx_id != ctx_id) {
+    // the lookup also creates and makes current the device's primary
+    // context when none was current, so the ID is read after it
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_on_device[dev] = static_cast<float*>(p);
+    e = current_context_id(&ctx_id);
+    if (e != cudaSuccess) return e;
+    if (ctx_id == 0) return cudaErrorDeviceUninitialized;
+    slot.ptr = static_cast<float*>(p);
+    slot.ctx_id = ctx_id;
   }
-  *out = g_scratch_on_device[dev];
+  *out = slot.ptr;
   return cudaSuccess;
 }
 
@@ -67,13 +116,17 @@ extern "C" int mha_decode_noalloc(const void* q, const void* Kcache, const void*
 
   const int nsm = mha::device_sm_count();
   if (nsm <= 0) return mha::record_cuda_failure(cudaGetLastError());
-  const int nsplit = mha::decode_num_splits(B, H, nsm);
+  // mha_decode's split count, lowered until the partials fit in the array;
+  // one split needs no scratch at all (the split kernel writes O itself)
+  const size_t per_split = static_cast<size_t>(B) * H * (D + 2);
+  int nsplit = mha::decode_num_splits(B, H, nsm);
+  if (static_cast<size_t>(nsplit) * per_split > kScratchFloats)
+    nsplit = static_cast<int>(kScratchFloats / per_split);
+  if (nsplit < 1) nsplit = 1;
   float* ws = nullptr;
   if (nsplit > 1) {
     // every partial slot is written by the split kernel before the merge
     // reads it, so nothing left in the array by an earlier call is used
-    const size_t need = static_cast<size_t>(B) * H * nsplit * (D + 2);
-    if (need > kScratchFloats) return MHA_ERR_UNSUPPORTED;
     const cudaError_t e = scratch_address(&ws);
     if (e != cudaSuccess) return mha::record_cuda_failure(e);
   }

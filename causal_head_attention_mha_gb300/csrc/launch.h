@@ -27,7 +27,9 @@ cudaError_t launch_prefill_f32(const float* Q, const float* K, const float* V, f
                                float* LSE, int B, int H, int S, int D, float scale, int causal,
                                cudaStream_t stream);
 
-// Number of key splits mha_decode uses for a given batch and head count.
+// Number of key splits mha_decode uses for a given batch and head count
+// (1..kMaxDecodeSplits).
+constexpr int kMaxDecodeSplits = 64;
 int decode_num_splits(int B, int H, int num_sms);
 
 // Partials of the key splits go to `ws` (B*H*nsplit*(D+2) floats, ignored when nsplit == 1).

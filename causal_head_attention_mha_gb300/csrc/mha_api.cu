@@ -140,8 +140,10 @@ int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float*
 
 namespace {
 
+// nsplit_req: 0 = automatic (mha::decode_num_splits), else 1..kMaxDecodeSplits.
 int decode_impl(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
-                void* O, int B, int H, int D, float scale, void* stream, bool f16) {
+                void* O, int B, int H, int D, float scale, void* stream, bool f16,
+                int nsplit_req) {
   if (!q || !Kcache || !Vcache || !seqlens || !O) return MHA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || D < 1) return MHA_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || scale == INFINITY) return MHA_ERR_INVALID_ARG;
@@ -154,7 +156,7 @@ int decode_impl(const void* q, const void* Kcache, const void* Vcache, const int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int nsm = mha::device_sm_count();
   if (nsm <= 0) return cuda_fail(cudaGetLastError());
-  const int nsplit = mha::decode_num_splits(B, H, nsm);
+  const int nsplit = nsplit_req > 0 ? nsplit_req : mha::decode_num_splits(B, H, nsm);
   float* ws = nullptr;
   if (nsplit > 1) {
     const size_t bytes = static_cast<size_t>(B) * H * nsplit * (D + 2) * sizeof(float);
@@ -176,12 +178,20 @@ extern "C" {
 
 int mha_decode(const void* q, const void* Kcache, const void* Vcache, const int* seqlens, void* O,
                int B, int H, int D, float scale, void* stream) {
-  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, false);
+  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, false, 0);
 }
 
 int mha_decode_f16(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
                    void* O, int B, int H, int D, float scale, void* stream) {
-  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, true);
+  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, true, 0);
+}
+
+int mha_decode_ex(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
+                  void* O, int B, int H, int D, float scale, int nsplit, int dtype,
+                  void* stream) {
+  if (nsplit < 0 || nsplit > mha::kMaxDecodeSplits) return MHA_ERR_INVALID_ARG;
+  if (dtype != 0 && dtype != 1) return MHA_ERR_UNSUPPORTED;
+  return decode_impl(q, Kcache, Vcache, seqlens, O, B, H, D, scale, stream, dtype == 1, nsplit);
 }
 
 int mha_qkv_proj(const void* X, const void* W, void* Q, void* K, void* V, int B, int S,

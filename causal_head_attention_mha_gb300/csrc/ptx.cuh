@@ -5,8 +5,6 @@
 #include <cstdint>
 #include <cuda.h>
 
-#include "exp2_poly.h"
-
 namespace mha {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -494,26 +492,6 @@ __device__ __forceinline__ float add_f16_hi(uint32_t w, float acc) {
   asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
       : "=f"(d) : "r"(w), "f"(acc));
   return d;
-}
-
-// 2^x for a pair, on the FMA pipe: x = n + f with n = round(x) (the 1.5*2^23
-// shifter leaves n in the low mantissa bits), 2^f from the degree-3 minimax
-// polynomial of exp2_poly.h, then n is added to the exponent field.  x is
-// clamped to [-126, 127] so the exponent add cannot leave the normal range.
-// Relative error <= 7.5e-5 plus fp32 rounding.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  x.x = fminf(fmaxf(x.x, -126.0f), 127.0f);
-  x.y = fminf(fmaxf(x.y, -126.0f), 127.0f);
-  const float2 t = add2(x, make_float2(kShift, kShift));
-  const float2 n = add2(t, make_float2(-kShift, -kShift));
-  const float2 f = fma2(n, make_float2(-1.0f, -1.0f), x);
-  float2 p = fma2(make_float2(MHA_EXP2_POLY_C3, MHA_EXP2_POLY_C3), f,
-                  make_float2(MHA_EXP2_POLY_C2, MHA_EXP2_POLY_C2));
-  p = fma2(p, f, make_float2(MHA_EXP2_POLY_C1, MHA_EXP2_POLY_C1));
-  p = fma2(p, f, make_float2(MHA_EXP2_POLY_C0, MHA_EXP2_POLY_C0));
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
 // two floats -> packed bf16x2, `lo` in the low half (round to nearest even)

@@ -105,6 +105,10 @@ int mha_fwd_varlen_f16(const void* Q, const void* K, const void* V, void* O, flo
 /*
  * The same operation with float32 inputs and outputs, computed in fp32 on
  * the CUDA cores (no reduced-precision tensor-core arithmetic anywhere).
+ * Page 3 ("Hand-written masked multi-head attention CUDA kernel"), section 2
+ * defines the operation and section 3.3 the precision split this path drops:
+ * there the operands are stored in 16 bits and the arithmetic is fp32; here
+ * storage and arithmetic are both fp32, the parity path for fp32 inputs.
  * Arguments as mha_fwd, with Q, K, V, O float [B, H, S, D].  D : 64 or 128.
  */
 int mha_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
@@ -142,6 +146,25 @@ int mha_decode_f16(const void* q, const void* Kcache, const void* Vcache, const 
                    void* O, int B, int H, int D, float scale, void* stream);
 
 /*
+ * mha_decode / mha_decode_f16 with the number of key splits chosen by the
+ * caller.  The split count changes only how the keys of a row are divided
+ * among thread blocks before the log-sum-exp merge (page 1, "Week 4 CUDA
+ * notes", section 2.2: the blocks' normalisations are reconciled, never
+ * applied per block), so every split count gives the same attention up to
+ * fp32 rounding; this call lets a caller (or a test) pick it.
+ *
+ *   nsplit : 0 = the automatic choice of mha_decode (mha_decode_num_splits);
+ *            1..64 = that many splits (1 = one block per row, no merge
+ *            kernel, no scratch).  Other values: MHA_ERR_INVALID_ARG.
+ *   dtype  : 0 = bf16, 1 = f16 (q, Kcache, Vcache and O); others
+ *            MHA_ERR_UNSUPPORTED.
+ *   other arguments, scratch and errors as mha_decode.
+ */
+int mha_decode_ex(const void* q, const void* Kcache, const void* Vcache, const int* seqlens,
+                  void* O, int B, int H, int D, float scale, int nsplit, int dtype,
+                  void* stream);
+
+/*
  * mha_decode without allocating anything.  This entry point has no
  * counterpart on the pages the method comes from; it exists for callers
  * that cannot allocate device memory when they call: a serving loop that
@@ -154,13 +177,19 @@ int mha_decode_f16(const void* q, const void* Kcache, const void* Vcache, const 
  * partials go to one file-scope device array of
  * MHA_DECODE_NOALLOC_SCRATCH_BYTES (2 MiB) that every GPU which loads the
  * library holds until the process exits; the call itself makes no
- * cudaMalloc/cudaFree or other allocating call.  When the partials would
- * not fit (B*H*splits*(D+2)*4 bytes > 2 MiB, see mha_decode_num_splits) the
- * call returns MHA_ERR_UNSUPPORTED before launching anything.
+ * cudaMalloc/cudaFree or other allocating call.  It uses mha_decode's split
+ * count (mha_decode_num_splits) when the partials, B*H*splits*(D+2)*4
+ * bytes, fit in the array, and otherwise the largest split count whose
+ * partials fit, down to one split, which needs no scratch; the results
+ * agree with mha_decode's to fp32 rounding (bit for bit when the split
+ * count is the same).
  *
- * The first call on a device looks up that device's address of the array
- * (cudaGetSymbolAddress, with the device current); make that first call
- * before any stream capture.  All calls share the one array and it keeps
+ * The first call in a CUDA context looks up the array's address in that
+ * context (cudaGetSymbolAddress, with the device current) and keeps it
+ * together with the context's unique ID; a call after the context was
+ * destroyed and created again (cudaDeviceReset) looks it up again.  Make
+ * the first call on a device, and the first after a reset, before any
+ * stream capture.  All calls share the one array and it keeps
  * whatever the last call left there; no part of it has to start at zero,
  * since every slot a call reads was written earlier in that same call.
  * Calls that overlap on the GPU (for instance on two streams) race on the

@@ -96,16 +96,23 @@ def _scale_keys(t, lo, hi, factor):
 
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("which", ["later_keys_dominate", "first_keys_dominate"])
+@pytest.mark.parametrize("which", ["later_keys_dominate", "first_keys_dominate",
+                                   "second_half_dominates"])
 def test_bf16_prefill_reference_moves(causal, D, which):
     """Scores of some keys far above the others (x64): with later keys larger,
     a row's reference maximum has to move by far more than 64 (log2 units)
-    after its first tile, which takes the kernel's re-do path (true maximum
-    from tensor memory, O rescaled); with the first keys larger, later tiles
-    underflow against the reference."""
+    after its first tile, which takes the kernel's re-do path (the tile's
+    weights redone with its true maximum, O rescaled); with the first keys
+    larger, later tiles underflow against the reference.  With only keys
+    192..255 larger (the second half of key tile 1), the first half of that
+    tile stays within the bound and is handed to the tensor core before the
+    second half is found to pass it: the second half is redone and O, which
+    by then includes the first half's product, is rescaled after that
+    product completes."""
     S = 300
     x = si.prefill_inputs(1, 2, S, D, seed=777 + D)
-    lo, hi = (128, S) if which == "later_keys_dominate" else (0, 128)
+    lo, hi = {"later_keys_dominate": (128, S), "first_keys_dominate": (0, 128),
+              "second_half_dominates": (192, 256)}[which]
     K = _scale_keys(x.K, lo, hi, 64.0)
     O, L = mha().mha_fwd(dev_tensor(x.Q, torch.bfloat16), dev_tensor(K, torch.bfloat16),
                          dev_tensor(x.V, torch.bfloat16), scale=x.scale, causal=causal)
