@@ -26,7 +26,10 @@
 //   warps 4..7   softmax of tile A, one query row per thread (128 keys per
 //                row and tile), P_A,j written as bf16 over the columns of
 //                S_A,j; rescales O_A when the row's reference maximum moves;
-//                item epilogue O_A / l, log-sum-exp
+//                item epilogue O_A / l, log-sum-exp.  On f16 data and at
+//                D = 64, P_A,j is handed to the MMA thread in two halves
+//                (keys 0..63, then 64..127), so the product of the first
+//                half with V runs while the second half is computed.
 //   warps 8..11  the same for tile B
 // The issuer orders each key step as P_A,j-1 V_j-1, S_A,j, P_B,j-1 V_j-1,
 // S_B,j: while one tile's softmax runs, the tensor pipe executes the other
@@ -98,8 +101,13 @@ struct Cfg {
   static constexpr int B_FULL = 4;                 // [unit] its tiles landed
   static constexpr int B_EMPTY = B_FULL + NUNIT;   // [unit] their last reader complete
   static constexpr int B_SFULL = B_EMPTY + NUNIT;  // [X] S_X,j in TMEM
-  static constexpr int B_PFULL = B_SFULL + 2;     // [X] P_X,j in TMEM, O_X rescaled (128 arrivals)
-  static constexpr int B_OFULL = B_PFULL + 2;     // [X] the item's last P_X V complete
+  // P_X,j is handed over in two halves where the kernel splits it: keys
+  // 0..63 (P_LO, once O_X is rescaled) and keys 64..127 (P_HI), so the
+  // product of the first half runs while the softmax threads compute the
+  // second; unsplit, P_LO carries the whole tile and P_HI is unused
+  static constexpr int B_PLO = B_SFULL + 2;       // [X] P_X,j keys 0..63 (or all) in TMEM (128 arrivals)
+  static constexpr int B_PHI = B_PLO + 2;         // [X] P_X,j keys 64..127 in TMEM (128 arrivals)
+  static constexpr int B_OFULL = B_PHI + 2;       // [X] the item's last P_X V complete
   static constexpr int B_OFREE = B_OFULL + 2;     // [X] O_X read by the epilogue (128 arrivals)
   static constexpr int B_DRAIN = B_OFREE + 2;     // every MMA complete
   static constexpr int NBAR = B_DRAIN + 1;
@@ -118,7 +126,8 @@ struct Cfg {
 // sites recorded with a timeout (bits 8.. of the error word)
 enum : uint32_t {
   SITE_PROD_EMPTY = 1, SITE_PROD_QEMPTY, SITE_MMA_Q, SITE_MMA_KFULL, SITE_MMA_VFULL,
-  SITE_MMA_PFULL, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL, SITE_WATCH_FULL, SITE_WATCH_PFULL
+  SITE_MMA_PLO, SITE_MMA_OFREE, SITE_SM_SFULL, SITE_SM_OFULL, SITE_WATCH_FULL, SITE_WATCH_PLO,
+  SITE_MMA_PHI
 };
 
 // The K/V units each key step reads, walked in the order the producer fills
@@ -248,9 +257,11 @@ struct Elem;
 template <>
 struct Elem<false> {  // bf16
   static constexpr uint32_t kOne = 0x3F80u;  // 1.0
-  // Largest fp32 weight sum of one tile kept without moving the reference
-  // maximum (2^64): every weight is then <= 2^64, far inside fp32 and bf16 range.
+  // Largest fp32 weight sum of one half tile (64 keys) kept without moving
+  // the reference maximum (2^64): every weight is then <= 2^64, far inside
+  // fp32 and bf16 range.
   static constexpr float kMaxTileWeight = 18446744073709551616.0f;
+  static constexpr float kMaxLog2Weight = 64.0f;  // the same bound for one weight, log2 units
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
   static __device__ __forceinline__ float add_lo(uint32_t w, float a) { return add_bf16_lo(w, a); }
   static __device__ __forceinline__ float add_hi(uint32_t w, float a) { return add_bf16_hi(w, a); }
@@ -277,6 +288,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
                                              int o_bshd, uint64_t wait_limit_ns, int inject) {
   using C = Cfg<D>;
   using E = Elem<F16>;
+  // Hand P_X,j over in two halves (the first half's product with V runs
+  // while the softmax threads compute the second) where that measured
+  // faster: f16 data, and bf16 at D = 64.  bf16 at D = 128 hands the whole
+  // tile over at once (measured 5-7 % faster there).
+  constexpr bool SPLIT = F16 || D == 64;
   // valid keys of the sequence of (b, h) = bh: key_lens[b] clamped to [0, S]
   // with key padding (VARLEN), else S
   // element offset of row (bh, q) of O: [B, H, S, D], or [B, S, H, D] when
@@ -312,8 +328,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       mbar_init(bar(C::B_QFULL + x), 1);
       mbar_init(bar(C::B_QEMPTY + x), 1);
       mbar_init(bar(C::B_SFULL + x), 1);
-      // tile A: one more arrival, from the operand watcher (warp 3)
-      mbar_init(bar(C::B_PFULL + x), (x == 0 && C::WATCH) ? 129 : 128);
+      // tile A's first half: one more arrival, from the operand watcher (warp 3)
+      mbar_init(bar(C::B_PLO + x), (x == 0 && C::WATCH) ? 129 : 128);
+      mbar_init(bar(C::B_PHI + x), 128);
       mbar_init(bar(C::B_OFULL + x), 1);
       mbar_init(bar(C::B_OFREE + x), 128);
     }
@@ -457,18 +474,18 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       // keys 64..127 of V start 64 rows (8 KB) further
       constexpr uint32_t kVHalf = C::ONES ? 512u - (512u << 16) : 512u;
       auto full_bar = [&](uint32_t pos) { return bar(C::B_FULL + static_cast<int>(pos >> 1)); };
-      // O_X (+)= P_X V_j-1: V MN-major, LBO = next 64 columns of D, keys
-      // 64.. start 64 rows (8 KB) into each block
-      auto issue_pv = [&](int x, uint32_t acc) {
-        const uint32_t v_lo = ring_lo + kVLo + (ring.vpos >> 1) * kVSlot;
-        const uint32_t tO = tmem + C::TM_O + x * C::O_STRIDE, tP = tmem + C::TM_S + x * 128;
-        if constexpr (C::ONES) {
+      // O_X (+)= P_X V_j-1 over one half of the keys (h = 0: keys 0..63, h = 1:
+      // keys 64..127): V MN-major, LBO = next 64 columns of D; keys 64.. start
+      // 64 rows (8 KB) into each block; P_X's half h is TMEM columns 32h..32h+31
+      // of S_X (bf16 pairs)
+      auto issue_pv = [&](int x, int h, uint32_t acc) {
+        const uint32_t v_lo = ring_lo + kVLo + (ring.vpos >> 1) * kVSlot + (h ? kVHalf : 0u);
+        const uint32_t tO = tmem + C::TM_O + x * C::O_STRIDE;
+        const uint32_t tP = tmem + C::TM_S + x * 128 + (h ? 32u : 0u);
+        if constexpr (C::ONES)
           umma_ts_mnmajor_x4_b1fixed(tO, tP, desc(v_lo), idesc_o, acc);
-          umma_ts_mnmajor_x4_b1fixed(tO, tP + 32, desc(v_lo + kVHalf), idesc_o, 1u);
-        } else {
+        else
           umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
-          umma_ts_mnmajor_x4(tO, tP + 32, desc(v_lo + kVHalf), idesc_o, 1u);
-        }
       };
       // S_X = Q_X K_j^T (K-major operands, LBO unused), then S_FULL[X]
       auto issue_s = [&](int x) {
@@ -490,27 +507,39 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
         const int jf = min(nx[0], nx[1]) - 1;
         for (int j = 0; ok && j <= sh.nkv; ++j) {
           if (j >= 2 && j < jf) {
-            // ---- steady step: "P_A ready" also says this step's K and V
-            // landed (the watcher's arrival)
+            // ---- steady step: "P_A ready" (its first half, when split) also
+            // says this step's K and V landed (the watcher's arrival)
             ring.step(true, true);
             if constexpr (C::WATCH) {
-              ok = mbar_wait(bar(C::B_PFULL), bit(0), wc, SITE_MMA_PFULL);
+              ok = mbar_wait(bar(C::B_PLO), bit(0), wc, SITE_MMA_PLO);
             } else {
               // paired units: V_j-1 shares the unit of K_j-1, checked at the
               // previous step; K_j and P_A are probed together
-              const uint32_t bk = full_bar(ring.kpos), bpa = bar(C::B_PFULL);
+              const uint32_t bk = full_bar(ring.kpos), bpa = bar(C::B_PLO);
               if (!mbar_test2(bk, ring.kpos & 1, bpa, bit(0)))
                 ok = mbar_wait(bk, ring.kpos & 1, wc, SITE_MMA_KFULL) &&
-                     mbar_wait(bpa, bit(0), wc, SITE_MMA_PFULL);
+                     mbar_wait(bpa, bit(0), wc, SITE_MMA_PLO);
             }
             if (!ok) break;
             tc_fence_after();
-            issue_pv(0, 1u);
+            issue_pv(0, 0, 1u);
+            if constexpr (SPLIT) {
+              ok = mbar_wait(bar(C::B_PHI), bit(0), wc, SITE_MMA_PHI);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_pv(0, 1, 1u);
             issue_s(0);
-            ok = mbar_wait(bar(C::B_PFULL + 1), bit(1), wc, SITE_MMA_PFULL);
+            ok = mbar_wait(bar(C::B_PLO + 1), bit(1), wc, SITE_MMA_PLO);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(1, 1u);
+            issue_pv(1, 0, 1u);
+            if constexpr (SPLIT) {
+              ok = mbar_wait(bar(C::B_PHI + 1), bit(1), wc, SITE_MMA_PHI);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_pv(1, 1, 1u);
             // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1)
             umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.vpos >> 1)));
             issue_s(1);
@@ -522,7 +551,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           // ---- general step (item start and end, ragged tiles)
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
           ring.step(pv_step, s_step);
-          // Operand waits, where "P_A ready" does not already cover them (no
+          // Operand waits, where "P_A,lo ready" does not already cover them (no
           // P_A V at this step); a paired unit was waited for when its K was
           // needed
           if (!C::WATCH || !(pv_step && j - 1 < nx[0])) {
@@ -532,14 +561,20 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           }
           for (int x = 0; ok && x < 2; ++x) {
             if (pv_step && j - 1 < nx[x]) {
-              ok = mbar_wait(bar(C::B_PFULL + x), bit(x), wc, SITE_MMA_PFULL);
+              ok = mbar_wait(bar(C::B_PLO + x), bit(x), wc, SITE_MMA_PLO);
               // O_X was last read by the previous item's epilogue (O_X items
               // parity flipped since, so the wanted phase is its complement)
               if (ok && j == 1 && bit(6 + x))
                 ok = mbar_wait(bar(C::B_OFREE + x), bit(4 + x) ^ 1u, wc, SITE_MMA_OFREE);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(x, j > 1 ? 1u : 0u);
+              issue_pv(x, 0, j > 1 ? 1u : 0u);
+              if constexpr (SPLIT) {
+                ok = mbar_wait(bar(C::B_PHI + x), bit(x), wc, SITE_MMA_PHI);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_pv(x, 1, 1u);
               ph ^= 1u << x;
               if (j - 1 == nx[x] - 1) umma_commit(bar(C::B_OFULL + x));
             }
@@ -563,7 +598,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
   } else {
     // ------------------------------------------------------------ operand watcher
     // Every key step whose products include P_A,j-1 V_j-1 starts with the
-    // MMA thread's wait for "P_A ready".  This warp makes that one wait
+    // MMA thread's wait for "P_A,lo ready".  This warp makes that one wait
     // also cover the step's K and V units: it waits until they have landed
     // and then adds its own arrival to that phase (which so needs 129), so
     // the MMA thread checks no ring barrier in those steps.  It arrives for
@@ -572,9 +607,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       Sched<D == 64> sch(n_qp, BH, CAUSAL);
       RingWalk<C::NUNIT, C::PAIRED> ring;
       int bh, qp;
-      uint32_t pa = 0;  // phase parity of "P_A ready"
+      uint32_t pa = 0;  // phase parity of "P_A,lo ready"
       bool ok = true;
-      const uint32_t pfull_a = bar(C::B_PFULL);
+      const uint32_t pfull_a = bar(C::B_PLO);
       while (ok && sch.next(bh, qp)) {
         const ItemShape sh(qp, S, key_len(bh), CAUSAL);
         for (int j = 0; ok && j <= sh.nkv; ++j) {
@@ -589,7 +624,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
                            SITE_WATCH_FULL);
           if (!ok) break;
           mbar_arrive(pfull_a);
-          ok = mbar_wait(pfull_a, pa, wc, SITE_WATCH_PFULL);
+          ok = mbar_wait(pfull_a, pa, wc, SITE_WATCH_PLO);
           pa ^= 1u;
         }
       }
@@ -606,7 +641,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
     const uint32_t tO = tmem + lane_base + C::TM_O + x * C::O_STRIDE;
-    const uint32_t sfull = bar(C::B_SFULL + x), pfull = bar(C::B_PFULL + x);
+    const uint32_t sfull = bar(C::B_SFULL + x), plo = bar(C::B_PLO + x), phi = bar(C::B_PHI + x);
     Sched<D == 64> sch(n_qp, BH, CAUSAL);
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
     bool failed = false;
@@ -629,123 +664,260 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       float m_run = -INFINITY;  // reference maximum, log2 units
       float l_run = 0.f;        // sum of fp32 weights: gives the log-sum-exp
       float lp_run = 0.f;       // sum of bf16-rounded weights: normalises O
-      for (int j = 0; j < nx; ++j, ++ns) {
-        failed = !__all_sync(0xffffffffu, mbar_wait(sfull, ns & 1, wc, SITE_SM_SFULL));
-        if (failed) break;
-        tc_fence_after();
-        uint32_t s[128];
-        tmem_ld_32x32b_x128(tS, s);
-        const bool need_mask = CAUSAL ? (j == nx - 1) : (j * BN + BN > L);
-        // last key index (within this tile) the row may use
-        const int lim = (CAUSAL ? min(q, L - 1) : (L - 1)) - j * BN;
-        auto mask = [&](uint32_t (&v)[128]) {
+      if constexpr (SPLIT) {
+        for (int j = 0; j < nx; ++j, ++ns) {
+          failed = !__all_sync(0xffffffffu, mbar_wait(sfull, ns & 1, wc, SITE_SM_SFULL));
+          if (failed) break;
+          tc_fence_after();
+          uint32_t s[128];
+          tmem_ld_32x32b_x128(tS, s);
+          const bool need_mask = CAUSAL ? (j == nx - 1) : (j * BN + BN > L);
+          // last key index (within this tile) the row may use
+          const int lim = (CAUSAL ? min(q, L - 1) : (L - 1)) - j * BN;
+          auto mask = [&](uint32_t (&v)[128]) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i > lim) v[i] = __float_as_uint(-INFINITY);
-        };
-        // row maximum in log2 units: eight independent chains, three-input max.
-        // Every row keeps at least its own key (causal) or key 0: it is finite.
-        auto row_max = [&](const uint32_t (&v)[128]) {
-          float m8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[k]), __uint_as_float(v[k + 8]));
-#pragma unroll
-          for (int i = 16; i < 128; i += 16)
+            for (int i = 0; i < 128; ++i)
+              if (i > lim) v[i] = __float_as_uint(-INFINITY);
+          };
+          // maximum of keys [K0, K0 + 16 * G) of the row in log2 units: eight
+          // independent chains, three-input max.  Every row keeps at least its
+          // own key (causal) or key 0, so the whole row's maximum is finite.
+          auto row_max = [&](const uint32_t (&v)[128], const int K0, const int G) {
+            float m8[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              m8[k] = max3f(m8[k], __uint_as_float(v[i + k]), __uint_as_float(v[i + 8 + k]));
-          return c_log2 * max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
-                                fmaxf(m8[6], m8[7]));
-        };
-        if (need_mask) mask(s);
-        // Reference maximum m_use: the row maximum on an item's first tile;
-        // afterwards the running reference is kept as long as no weight of the
-        // tile exceeds 2^64 (checked through the tile's weight sum).  Weights up
-        // to 2^64 are exact in fp32 and bf16 range and their sums cannot
-        // overflow, so the row maximum of later tiles is never needed in the
-        // common case.  Softmax does not depend on the reference, so this is
-        // exact arithmetic.  A tile that does overflow (its scores exceed the
-        // reference by ~64, log2 units) is redone from tensor memory with its
-        // true maximum, and O is rescaled.  (That is the bf16 path; the f16
-        // path, whose weights must stay <= 2^15, takes every tile's row
-        // maximum instead: see Elem<true>.)
-        const bool first = (j == 0);
-        float m_use = first ? row_max(s) : m_run;
-        if constexpr (F16) {
-          if (!first) {
-            const float mx = row_max(s);
-            if (mx > m_run + E::kHeadroom) m_use = mx;
+              m8[k] = fmaxf(__uint_as_float(v[K0 + k]), __uint_as_float(v[K0 + k + 8]));
+#pragma unroll
+            for (int g = 1; g < G; ++g)
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                m8[k] = max3f(m8[k], __uint_as_float(v[K0 + 16 * g + k]),
+                              __uint_as_float(v[K0 + 16 * g + 8 + k]));
+            return c_log2 * max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                                  fmaxf(m8[6], m8[7]));
+          };
+          if (need_mask) mask(s);
+          // Reference maximum m_use: the row maximum on an item's first tile;
+          // afterwards the running reference is kept as long as no weight of the
+          // tile exceeds 2^64: checked for keys 0..63 through their fp32 weight
+          // sum, and for keys 64..127 -- whose weights are computed only after
+          // keys 0..63 have been handed to the tensor core -- through their
+          // maximum.  Weights up to 2^64 are exact in fp32 and inside bf16's
+          // range and their sums cannot overflow, so the row maximum of the
+          // whole tile is not needed in the common case.  Softmax does not
+          // depend on the reference, so this is exact arithmetic.  A tile that
+          // passes the bound (scores above the reference by ~64, log2 units)
+          // is redone from its scores with its true maximum, and O is rescaled,
+          // before any of its weights are handed over.  (That is the bf16
+          // path; the f16 path, whose weights must stay <= 2^15, takes every
+          // tile's row maximum instead: see Elem<true>.)
+          const bool first = (j == 0);
+          float m_use = first ? row_max(s, 0, 8) : m_run;
+          if constexpr (F16) {
+            if (!first) {
+              const float mx = row_max(s, 0, 8);
+              if (mx > m_run + E::kHeadroom) m_use = mx;
+            }
           }
-        }
-        const float2 c2 = make_float2(c_log2, c_log2);
-        // P_X,j and its partial sums: the fp32 weights (for the log-sum-exp and
-        // the overflow check) and the bf16-rounded weights the P.V product uses
-        // (to normalise O, so that O is an exact convex combination of V rows)
-        uint32_t pk[2][32];
-        float rs, rsp;
-#pragma unroll 1
-        for (int pass = 0;; ++pass) {
-          const float2 nm2 = make_float2(-m_use, -m_use);
-          float2 se[4];
-          float sr[8];
+          const float2 c2 = make_float2(c_log2, c_log2);
+          // P_X,j for keys 64h .. 64h + 63 (packed pairs) and its partial sums:
+          // the fp32 weights (for the log-sum-exp and the overflow check) and
+          // the bf16-rounded weights the P.V product uses (to normalise O, so
+          // that O is an exact convex combination of V rows)
+          auto half_exp = [&](const int h, const float m, uint32_t (&pk)[32], float& rs, float& rsp) {
+            const float2 nm2 = make_float2(-m, -m);
+            float2 se[4];
+            float sr[8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
+            for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) sr[k] = 0.f;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
+            for (int k = 0; k < 8; ++k) sr[k] = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int e0 = 64 * h + 2 * i;
-              const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
-                                    c2, nm2);
+              const float2 v =
+                  fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])), c2, nm2);
               const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
-              pk[h][i] = E::pack(e.x, e.y);
+              pk[i] = E::pack(e.x, e.y);
               se[i & 3] = add2(se[i & 3], e);
               if constexpr (!C::ONES) {
-                sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
-                sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+                sr[(i & 3) * 2] = E::add_lo(pk[i], sr[(i & 3) * 2]);
+                sr[(i & 3) * 2 + 1] = E::add_hi(pk[i], sr[(i & 3) * 2 + 1]);
               }
             }
+            se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
+            rs = se[0].x + se[0].y;
+            rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+          };
+          uint32_t pk[32];
+          float rs0, rsp0;
+          half_exp(0, m_use, pk, rs0, rsp0);
+          if constexpr (!F16) {
+            // keys 0..63 through their weight sum (also NaN / inf sums), keys
+            // 64..127 through their maximum
+            const bool redo = !first && (!(rs0 <= E::kMaxTileWeight) ||
+                                         row_max(s, 64, 4) > m_use + E::kMaxLog2Weight);
+            if (__any_sync(0xffffffffu, redo)) {
+              // rare: the true maximum of the tile's row (its scores are still
+              // in registers; no weight has been handed over yet)
+              if (redo) m_use = fmaxf(m_run, row_max(s, 0, 8));
+              half_exp(0, m_use, pk, rs0, rsp0);
+            }
           }
-          se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
-          rs = se[0].x + se[0].y;
-          rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
-          bool redo = false;
-          if constexpr (!F16) redo = pass == 0 && !first && !(rs <= E::kMaxTileWeight);  // also NaN / inf
-          if (!__any_sync(0xffffffffu, redo)) break;
-          // rare: the scores are still in tensor memory (P is stored below)
+          // P_X,j keys 0..63 over TMEM columns 0..31 of S_X,j, which this thread has read
+          tmem_st_32x32b_x32(tS, pk);
+          const bool resc = !first && (m_use != m_run);
+          if (__any_sync(0xffffffffu, resc)) {
+            // S_X,j complete implies P_X,j-1 V_j-1 complete (issued before it by
+            // the same thread), so O_X is final through tile j - 1 here.
+            const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
+#pragma unroll
+            for (int c = 0; c < (C::ON + 31) / 32; ++c) {  // with the weight-sum column
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(tO + c * 32, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st_32x32b_x32(tO + c * 32, o);
+            }
+            l_run *= alpha;
+            lp_run *= alpha;
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          // failure-detection test mode: the first "P ready" signal of tile A is
+          // withheld, so the MMA thread's bounded wait for it runs out
+          if (!(inject == 1 && x == 0 && ns == 0)) mbar_arrive(plo);
+          // keys 64..127 while the tensor core multiplies keys 0..63 into O_X
+          float rs1, rsp1;
+          half_exp(1, m_use, pk, rs1, rsp1);
+          tmem_st_32x32b_x32(tS + 32, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(phi);
+          l_run += rs0 + rs1;
+          lp_run += rsp0 + rsp1;
+          m_run = m_use;
+        }
+      } else {
+        // the whole tile's weights are handed over at once (first-half barrier)
+        for (int j = 0; j < nx; ++j, ++ns) {
+          failed = !__all_sync(0xffffffffu, mbar_wait(sfull, ns & 1, wc, SITE_SM_SFULL));
+          if (failed) break;
+          tc_fence_after();
+          uint32_t s[128];
           tmem_ld_32x32b_x128(tS, s);
+          const bool need_mask = CAUSAL ? (j == nx - 1) : (j * BN + BN > L);
+          // last key index (within this tile) the row may use
+          const int lim = (CAUSAL ? min(q, L - 1) : (L - 1)) - j * BN;
+          auto mask = [&](uint32_t (&v)[128]) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+              if (i > lim) v[i] = __float_as_uint(-INFINITY);
+          };
+          // row maximum in log2 units: eight independent chains, three-input max.
+          // Every row keeps at least its own key (causal) or key 0: it is finite.
+          auto row_max = [&](const uint32_t (&v)[128]) {
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[k]), __uint_as_float(v[k + 8]));
+#pragma unroll
+            for (int i = 16; i < 128; i += 16)
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                m8[k] = max3f(m8[k], __uint_as_float(v[i + k]), __uint_as_float(v[i + 8 + k]));
+            return c_log2 * max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                                  fmaxf(m8[6], m8[7]));
+          };
           if (need_mask) mask(s);
-          if (redo) m_use = fmaxf(m_run, row_max(s));
-        }
-        // P_X,j over the first 64 columns of S_X,j, which this thread has read
-        tmem_st_32x32b_x32(tS, pk[0]);
-        tmem_st_32x32b_x32(tS + 32, pk[1]);
-        const bool resc = !first && (m_use != m_run);
-        if (__any_sync(0xffffffffu, resc)) {
-          // S_X,j complete implies P_X,j-1 V_j-1 complete (issued before it by
-          // the same thread), so O_X is final through tile j - 1 here.
-          const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
-#pragma unroll
-          for (int c = 0; c < (C::ON + 31) / 32; ++c) {  // with the weight-sum column
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tO + c * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_32x32b_x32(tO + c * 32, o);
+          // Reference maximum m_use: the row maximum on an item's first tile;
+          // afterwards the running reference is kept as long as no weight of the
+          // tile exceeds 2^64 (checked through the tile's weight sum).  Weights up
+          // to 2^64 are exact in fp32 and bf16 range and their sums cannot
+          // overflow, so the row maximum of later tiles is never needed in the
+          // common case.  Softmax does not depend on the reference, so this is
+          // exact arithmetic.  A tile that does overflow (its scores exceed the
+          // reference by ~64, log2 units) is redone from tensor memory with its
+          // true maximum, and O is rescaled.  (That is the bf16 path; the f16
+          // path, whose weights must stay <= 2^15, takes every tile's row
+          // maximum instead: see Elem<true>.)
+          const bool first = (j == 0);
+          float m_use = first ? row_max(s) : m_run;
+          if constexpr (F16) {
+            if (!first) {
+              const float mx = row_max(s);
+              if (mx > m_run + E::kHeadroom) m_use = mx;
+            }
           }
-          l_run *= alpha;
-          lp_run *= alpha;
+          const float2 c2 = make_float2(c_log2, c_log2);
+          // P_X,j and its partial sums: the fp32 weights (for the log-sum-exp and
+          // the overflow check) and the bf16-rounded weights the P.V product uses
+          // (to normalise O, so that O is an exact convex combination of V rows)
+          uint32_t pk[2][32];
+          float rs, rsp;
+#pragma unroll 1
+          for (int pass = 0;; ++pass) {
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            float2 se[4];
+            float sr[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sr[k] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int e0 = 64 * h + 2 * i;
+                const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
+                                      c2, nm2);
+                const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
+                pk[h][i] = E::pack(e.x, e.y);
+                se[i & 3] = add2(se[i & 3], e);
+                if constexpr (!C::ONES) {
+                  sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
+                  sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+                }
+              }
+            }
+            se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
+            rs = se[0].x + se[0].y;
+            rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+            bool redo = false;
+            if constexpr (!F16) redo = pass == 0 && !first && !(rs <= E::kMaxTileWeight);  // also NaN / inf
+            if (!__any_sync(0xffffffffu, redo)) break;
+            // rare: the scores are still in tensor memory (P is stored below)
+            tmem_ld_32x32b_x128(tS, s);
+            if (need_mask) mask(s);
+            if (redo) m_use = fmaxf(m_run, row_max(s));
+          }
+          // P_X,j over the first 64 columns of S_X,j, which this thread has read
+          tmem_st_32x32b_x32(tS, pk[0]);
+          tmem_st_32x32b_x32(tS + 32, pk[1]);
+          const bool resc = !first && (m_use != m_run);
+          if (__any_sync(0xffffffffu, resc)) {
+            // S_X,j complete implies P_X,j-1 V_j-1 complete (issued before it by
+            // the same thread), so O_X is final through tile j - 1 here.
+            const float alpha = resc ? ex2_approx(m_run - m_use) : 1.0f;
+#pragma unroll
+            for (int c = 0; c < (C::ON + 31) / 32; ++c) {  // with the weight-sum column
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(tO + c * 32, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st_32x32b_x32(tO + c * 32, o);
+            }
+            l_run *= alpha;
+            lp_run *= alpha;
+          }
+          tmem_wait_st();
+          l_run += rs;
+          lp_run += rsp;
+          m_run = m_use;
+          tc_fence_before();
+          // failure-detection test mode: the first "P ready" signal of tile A is
+          // withheld, so the MMA thread's bounded wait for it runs out
+          if (!(inject == 1 && x == 0 && ns == 0)) mbar_arrive(plo);
         }
-        tmem_wait_st();
-        l_run += rs;
-        lp_run += rsp;
-        m_run = m_use;
-        tc_fence_before();
-        // failure-detection test mode: the first "P ready" signal of tile A is
-        // withheld, so the MMA thread's bounded wait for it runs out
-        if (!(inject == 1 && x == 0 && ns == 0)) mbar_arrive(pfull);
       }
       if (failed) break;
       // -------------------------------------------------------- epilogue of the item
