@@ -1,23 +1,34 @@
 #!/usr/bin/env python3
 """Throughput of the fused causal MHA path on GB300, one JSON line on stdout.
 
-A step is one pass of the hot path over one batch of synthetic input:
+A step is one pass of the hot path over one batch of synthetic input, every
+configuration of the workload table once, inputs resident in HBM:
   * bf16 causal prefill on the large-logit workload B=4, H=32, S=4096, D=128
-    (Q, K ~ N(0, 3^2), V ~ N(0, 1)) -- one mha_fwd call, O and LSE written;
+    (Q, K ~ N(0, 3^2), V ~ N(0, 1)) -- the headline: `value` and `roofline`;
+  * the same inputs with causal=0 (`prefill_noncausal`);
+  * bf16 causal prefill B=1, H=32, S=2048, D=128 (`prefill_s2048`);
+  * bf16 causal prefill B=2, H=16, S=16384, D=64 (`prefill_d64`);
+  * f16 causal prefill on the large-logit shape (`prefill_f16`) and bf16
+    causal prefill with key padding, lengths U{1024..4096} (`prefill_varlen`);
   * bf16 single-query decode on B=16, H=32, D=128 with cached lengths drawn
-    uniformly from [512, 8192] -- one mha_decode call (split + merge).
-`value` is the prefill throughput in TFLOP/s, counting 2*B*H*S^2*D flops per
-causal call, over the prefill kernels' device time; the decode throughput
-(algorithmic bytes: K and V read once, q read and O written) is reported in
-the `decode` object.  Inputs (384 MiB for prefill, ~1.1 GiB of cache for
-decode) are larger than the 129 MB L2, so no flush is needed between steps.
+    uniformly from [512, 8192] -- one mha_decode call (split + merge), in
+    the `decode` object.
+Prefill throughput counts 2*B*H*S^2*D flops per causal call (4*B*H*S^2*D
+without the mask; key padding counts each row's valid keys) over the device
+time of that configuration's launches, measured with CUDA events on the
+launching stream; decode counts algorithmic bytes (K and V read once, q read
+and O written).  Every configuration's inputs are larger than the 129 MB L2
+except the S=2048 one (50 MB of Q, K, V), which follows a launch of another
+configuration that streams more than L2 through it, so no flush is needed.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this build)
-on bounded samples of the same prefill workload, on the host cores.
+on bounded samples of the headline prefill workload, on the host cores.
+--gpus N (N > 1) without a launcher starts N ranks itself (torch.distributed.run).
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -41,46 +52,33 @@ DECODE_WORKLOAD = "decode_bf16_b16h32d128_len512_8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch measured with ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
-# named workload, valid only while the kernel source hashes to the recorded value.  The prefill
-# records come from one-pass captures (those metrics only) of `bench.py --only prefill
-# --prefill-workload <workload> --steps 1 --warmup 1 --profile`; the profiles named beside
-# them hold the full captures of the same kernels.
-TRAFFIC = {
-    # profiles/prefill_bf16_d128_causal_b4h32s4096.md
-    "prefill": {"kernel": "prefill_bf16", "workload": PREFILL_WORKLOAD,
-                "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 519273728},
-    # profiles/prefill_bf16_d64_causal_b2h16s16384.md
-    "prefill_d64": {"kernel": "prefill_bf16", "workload": "prefill_bf16_b2h16s16384d64",
-                    "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 345352960},
-    # profiles/prefill_f16_d128_causal_b4h32s4096.md
-    "prefill_f16": {"kernel": "prefill_f16", "workload": "prefill_f16_b4h32s4096d128_qk3",
-                    "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                    "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 522228992},
-    # key padding, B4 H32 S4096 D128 (one capture of the same bench command, dram metrics only)
-    "prefill_varlen": {"kernel": "prefill_bf16", "workload": "prefill_varlen_bf16_b4h32s4096d128",
-                       "files": ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                       "sha256": "34663ef60bd3ed993f66174c07c2bef1729c78e4dbf944c1358b3a7d8c979462", "bytes_per_launch": 453030656},
-    # profiles/decode_split_d128_b16h32_len512_8192.md (split kernel; merge adds ~4 MB)
-    "decode": {"kernel": "decode", "workload": DECODE_WORKLOAD, "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
-               "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1201886720},
-    # profiles/decode_split_f16_d128_b16h32_len512_8192.md
-    "decode_f16": {"kernel": "decode", "workload": "decode_f16_b16h32d128_len512_8192",
-                   "files": ['causal_head_attention_mha_gb300/csrc/decode.cu'],
-                   "sha256": "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", "bytes_per_launch": 1292623616},
-    # profiles/proj_gemm_bf16_b4s4096_h32d128.md (the projection kernels; these figures from one
-    # one-pass DRAM capture of `bench.py --only projections --steps 1 --warmup 1 --profile`)
-    "qkv_proj": {"kernel": "qkv_proj", "workload": "qkv_bf16_b4s4096hid4096_h32d128",
-                 "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                 "sha256": "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", "bytes_per_launch": 1354212608},
-    "out_proj_rows": {"kernel": "out_proj_rows", "workload": "outproj_bf16_b4h32s4096d128_n4096",
-                      "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                      "sha256": "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", "bytes_per_launch": 396940544},
-    "out_proj": {"kernel": "out_proj", "workload": "outproj_bf16_b4h32s4096d128_n4096",
-                 "files": ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu', 'causal_head_attention_mha_gb300/csrc/ptx.cuh'],
-                 "sha256": "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", "bytes_per_launch": 404913152},
-}
+# named workload, valid only while the kernel source hashes to the recorded value.  Each record
+# comes from a one-pass capture (those metrics only) of the `--only prefill | decode |
+# projections ... --steps 1 --warmup 1 --profile` bench command for that workload.
+PREFILL_SRC = ['causal_head_attention_mha_gb300/csrc/prefill_bf16.cu',
+               'causal_head_attention_mha_gb300/csrc/ptx.cuh']
+DECODE_SRC = ['causal_head_attention_mha_gb300/csrc/decode.cu']
+GEMM_SRC = ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu',
+            'causal_head_attention_mha_gb300/csrc/ptx.cuh']
+TRAFFIC = [
+    # kernel, workload, causal, sources, sha256 of the sources, bytes per launch
+    ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC, None, None),
+    ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC, None, None),
+    ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC, None, None),
+    ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC, None, None),
+    ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC, None, None),
+    ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC, None, None),
+    ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
+     "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", 1201886720),
+    ("decode", "decode_f16_b16h32d128_len512_8192", True, DECODE_SRC,
+     "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", 1292623616),
+    ("qkv_proj", "qkv_bf16_b4s4096hid4096_h32d128", True, GEMM_SRC,
+     "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", 1354212608),
+    ("out_proj_rows", "outproj_bf16_b4h32s4096d128_n4096", True, GEMM_SRC,
+     "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", 396940544),
+    ("out_proj", "outproj_bf16_b4h32s4096d128_n4096", True, GEMM_SRC,
+     "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", 404913152),
+]
 
 
 def source_sha(rels):
@@ -91,15 +89,15 @@ def source_sha(rels):
     return h.hexdigest()
 
 
-def traffic_for(kernel, workload):
+def traffic_for(kernel, workload, causal=True):
     """Recorded DRAM bytes per launch of `kernel` on `workload`, or None when no
     capture of this workload exists or the source changed since it was taken."""
-    for t in TRAFFIC.values():
-        if t["kernel"] != kernel or t["workload"] != workload:
+    for k, w, c, files, sha, nbytes in TRAFFIC:
+        if k != kernel or w != workload or c != causal:
             continue
-        if t["sha256"] is None or t["bytes_per_launch"] is None:
+        if sha is None or nbytes is None:
             return None
-        return t["bytes_per_launch"] if source_sha(t["files"]) == t["sha256"] else None
+        return nbytes if source_sha(files) == sha else None
     return None
 
 
@@ -169,24 +167,70 @@ def decode_bytes(B, H, D, seqlens):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of the SM clock, power and throttle reasons while the
+    GPU works; `mark` notes host times so the samples of the timed region can
+    be told from those of the soak before it."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=50):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
-        self.out = None
+        self.marks = {}
 
     def start(self):
         try:
-            self.out = open(os.devnull, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+
+    def mark(self, name):
+        self.marks[name] = datetime.datetime.now()
+
+    @staticmethod
+    def parse(text):
+        """(timestamp, sm MHz, max sm MHz, power W, active reasons) per CSV row."""
+        out = []
+        for r in text.strip().splitlines():
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                sm, smax = float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            try:
+                pw = float(f[4])
+            except ValueError:
+                pw = None
+            reasons = {n for n, v in zip(ClockSampler.REASONS, f[6:10]) if v.lower() == "active"}
+            out.append((ts, sm, smax, pw, reasons))
+        return out
+
+    @staticmethod
+    def summarise(rows, t0=None, t1=None):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [r[1] for r in rows]
+        load = [r for r in rows if r[1] > 0.5 * max(sm)] or rows
+        reasons = sorted(set().union(*(r[4] for r in load)))
+        pw = [r[3] for r in load if r[3] is not None]
+        d = {"sm_mhz": statistics.median(r[1] for r in load), "sm_max_mhz": max(r[2] for r in rows),
+             "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+             "power_w_max": max(pw) if pw else None}
+        if t0 is not None and t1 is not None:
+            timed = [r for r in rows if t0 <= r[0] <= t1]
+            d["samples_timed"] = len(timed)
+            d["sm_mhz_timed"] = statistics.median(r[1] for r in timed) if timed else None
+            d["reasons_timed"] = sorted(set().union(*(r[4] for r in timed))) if timed else []
+        return d
 
     def stop(self):
         if self.proc is None:
@@ -197,23 +241,8 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             text, _ = self.proc.communicate()
-        rows = [r.split(",") for r in text.strip().splitlines() if r.count(",") >= 8]
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-            except ValueError:
-                continue
-            for name, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        load = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarise(self.parse(text), self.marks.get("timed_start"),
+                              self.marks.get("timed_end"))
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -237,7 +266,7 @@ def oracle_sample_tflops(x, target_s, causal=True, seed=0, max_rows=None, worklo
     n = int(min(max_rows, max(64, target_s / per_row)))
     dt, flops, threads = run(n)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} random query rows of {workload} (causal), "
+            "sample": f"{n} random query rows of {workload} ({'causal' if causal else 'not causal'}), "
                       f"fp64 C oracle, {dt:.1f} s"}
 
 
@@ -288,6 +317,73 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ our arm
+# The prefill configurations of one step, in launch order: (key in the JSON line,
+# workload, causal).  The first is the headline (`value`).  The S = 2048 inputs
+# fit in L2; the launch before them streams more than L2 through it.
+PREFILL_CASES = [
+    ("prefill", PREFILL_WORKLOAD, True),
+    ("prefill_noncausal", PREFILL_WORKLOAD, False),
+    ("prefill_s2048", "prefill_bf16_b1h32s2048d128", True),
+    ("prefill_d64", "prefill_bf16_b2h16s16384d64", True),
+    ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True),
+    ("prefill_varlen", "prefill_varlen_bf16_b4h32s4096d128", True),
+]
+
+
+class PrefillCase:
+    """Device-resident inputs and outputs of one prefill configuration of the step."""
+
+    def __init__(self, mha, key, workload, causal, rank, dev, shared=None):
+        import torch
+        self.key, self.workload, self.causal = key, workload, causal
+        w = si.WORKLOADS[workload]
+        self.dtype = w["dtype"]
+        tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
+        self.varlen = "key_len_lo" in w
+        if shared is not None:  # the same inputs as another case (causal=0 on the headline data)
+            self.x, self.Q, self.K, self.V = shared.x, shared.Q, shared.K, shared.V
+        else:
+            self.x = si.prefill_inputs(w["B"], w["H"], w["S"], w["D"], rank_seed(w["seed"], rank),
+                                       qk_std=w["qk_std"], dtype=self.dtype)
+            self.Q, self.K, self.V = (torch.from_numpy(t.bits.view(np.int16)).view(tdt).to(dev)
+                                      for t in (self.x.Q, self.x.K, self.x.V))
+        x = self.x
+        self.O = torch.empty_like(self.Q)
+        self.LSE = torch.empty((x.B, x.H, x.S), dtype=torch.float32, device=dev)
+        self.KL = None
+        if self.varlen:
+            x.key_lens = si.prefill_key_lens(x.B, rank_seed(w["seed"], rank), w["key_len_lo"],
+                                             w["key_len_hi"])
+            self.KL = torch.from_numpy(x.key_lens).to(dev)
+            self.flops = prefill_flops_varlen(x.H, x.S, x.D, x.key_lens, causal)
+            self.fn = mha.mha_fwd_varlen_f16 if self.dtype == "f16" else mha.mha_fwd_varlen
+        else:
+            self.flops = prefill_flops(x.B, x.H, x.S, x.D, causal)
+            self.fn = mha.mha_fwd_f16 if self.dtype == "f16" else mha.mha_fwd
+        self.kernel_family = "prefill_" + self.dtype
+        self.kernel = (f"prefill_{self.dtype}{'_varlen' if self.varlen else ''}_kernel"
+                       f"<{x.D}, {'causal' if causal else 'not causal'}>")
+
+    def __call__(self, stream, O=None, LSE=None, Q=None, K=None, V=None):
+        args = (self.Q if Q is None else Q, self.K if K is None else K, self.V if V is None else V)
+        kw = dict(O=self.O if O is None else O, LSE=self.LSE if LSE is None else LSE,
+                  scale=self.x.scale, causal=self.causal, stream=stream)
+        if self.varlen:
+            self.fn(*args, self.KL, **kw)
+        else:
+            self.fn(*args, **kw)
+
+    def config(self):
+        x, w = self.x, si.WORKLOADS[self.workload]
+        c = {"workload": self.workload, "B": x.B, "H": x.H, "S": x.S, "D": x.D,
+             "causal": self.causal, "dtype": self.dtype, "qk_std": w["qk_std"],
+             "flops_per_step": self.flops}
+        if self.varlen:
+            c["key_lens"] = [int(v) for v in x.key_lens]
+            c["flops_count"] = "each row's valid keys, min(i + 1, L_b)"
+        return c
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import causal_head_attention_mha_gb300 as mha
@@ -299,53 +395,46 @@ def run_ours(args, rank, world, dist):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream(dev)
 
-    torch_dtype = {"bf16": torch.bfloat16, "f16": torch.float16}
-
-    def dev16(t, dtype):
-        return torch.from_numpy(t.bits.view(np.int16)).view(torch_dtype[dtype]).to(dev)
-
     do_prefill = args.only in ("both", "prefill")
     do_decode = args.only in ("both", "decode")
-    wp = si.WORKLOADS[args.prefill_workload]
-    wd = si.WORKLOADS[args.decode_workload]
-    pdt, ddt = wp["dtype"], wd.get("dtype", "bf16")
-    varlen = "key_len_lo" in wp
-    if varlen:
-        fwd = mha.mha_fwd_varlen_f16 if pdt == "f16" else mha.mha_fwd_varlen
+    # the prefill configurations of the step: every one by default, or the one named
+    if args.only == "both" and args.prefill_workload == PREFILL_WORKLOAD:
+        plan = PREFILL_CASES
     else:
-        fwd = mha.mha_fwd_f16 if pdt == "f16" else mha.mha_fwd
-    dec = mha.mha_decode_f16 if ddt == "f16" else mha.mha_decode
-    # each rank works on its own batch (weak scaling, no collective on the data path)
+        plan = [("prefill", args.prefill_workload, not args.noncausal)]
+    cases = []
     if do_prefill:
-        xp = si.prefill_inputs(wp["B"], wp["H"], wp["S"], wp["D"], rank_seed(wp["seed"], rank),
-                               qk_std=wp["qk_std"], dtype=pdt)
-        Q, K, V = dev16(xp.Q, pdt), dev16(xp.K, pdt), dev16(xp.V, pdt)
-        O = torch.empty_like(Q)
-        LSE = torch.empty((xp.B, xp.H, xp.S), dtype=torch.float32, device=dev)
-        if varlen:
-            xp.key_lens = si.prefill_key_lens(xp.B, rank_seed(wp["seed"], rank), wp["key_len_lo"],
-                                              wp["key_len_hi"])
-            KL = torch.from_numpy(xp.key_lens).to(dev)
-            flops = prefill_flops_varlen(xp.H, xp.S, xp.D, xp.key_lens, True)
-        else:
-            flops = prefill_flops(xp.B, xp.H, xp.S, xp.D, True)
+        for key, wl, causal in plan:
+            shared = next((c for c in cases if c.workload == wl), None)
+            cases.append(PrefillCase(mha, key, wl, causal, rank, dev, shared))
+    wd = si.WORKLOADS[args.decode_workload]
+    ddt = wd.get("dtype", "bf16")
+    dec = mha.mha_decode_f16 if ddt == "f16" else mha.mha_decode
     if do_decode:
         xd = si.decode_inputs(wd["B"], wd["H"], wd["D"], rank_seed(wd["seed"], rank), wd["len_lo"],
                               wd["len_hi"], dtype=ddt)
-        q, Kc, Vc = dev16(xd.q, ddt), dev16(xd.Kc, ddt), dev16(xd.Vc, ddt)
+        tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[ddt]
+        q, Kc, Vc = (torch.from_numpy(t.bits.view(np.int16)).view(tdt).to(dev)
+                     for t in (xd.q, xd.Kc, xd.Vc))
         sl = torch.from_numpy(xd.seqlens).to(dev)
         Od = torch.empty_like(q)
         dbytes = decode_bytes(xd.B, xd.H, xd.D, xd.seqlens)
         nsplit = mha.mha_decode_num_splits(xd.B, xd.H)
 
-    def prefill():
-        if varlen:
-            fwd(Q, K, V, KL, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
-        else:
-            fwd(Q, K, V, O=O, LSE=LSE, scale=xp.scale, causal=True, stream=stream)
-
     def decode():
         dec(q, Kc, Vc, sl, O=Od, scale=xd.scale, stream=stream)
+
+    def step(evs=None):
+        for i, c in enumerate(cases):
+            if evs is not None:
+                evs[i].record(stream)
+            c(stream)
+        if evs is not None:
+            evs[len(cases)].record(stream)
+        if do_decode:
+            decode()
+        if evs is not None:
+            evs[len(cases) + 1].record(stream)
 
     def barrier():
         if dist is not None:
@@ -354,45 +443,54 @@ def run_ours(args, rank, world, dist):
 
     # ---------------- warm-up
     for _ in range(args.warmup):
-        if do_prefill:
-            prefill()
-        if do_decode:
-            decode()
+        step()
     barrier()
     st = mha.mha_get_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {mha.mha_status_string(st)}")
 
-    # ---------------- timed region (device-resident inputs)
-    K_ = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
+    # ---------------- clock soak: back-to-back steps for about args.soak seconds, sampled
+    # together with the timed region, so the clock record has samples under load
     clock = ClockSampler(local)
+    soak_steps = 0
     if not args.profile:
         clock.start()
-        time.sleep(0.3)
+        time.sleep(0.2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        barrier()
+        one = max(e0.elapsed_time(e1) / 1e3, 1e-5)
+        soak_steps = int(math.ceil(args.soak / one))
+        for _ in range(soak_steps):
+            step()
+        barrier()
+
+    # ---------------- timed region (device-resident inputs)
+    K_ = args.steps
+    nev = len(cases) + 2
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K_)]
     barrier()
+    clock.mark("timed_start")
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(K_):
-        evs[k][0].record(stream)
-        if do_prefill:
-            prefill()
-        evs[k][1].record(stream)
-        if do_decode:
-            decode()
-        evs[k][2].record(stream)
+        step(evs[k])
     t_end.record(stream)
     barrier()
+    clock.mark("timed_end")
     clocks = clock.stop() if not args.profile else None
     st = mha.mha_get_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {mha.mha_status_string(st)}")
-    tp = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3  # s, prefill launches
-    td = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3  # s, decode launches
+    per_case = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / 1e3 for i in range(len(cases))]
+    td = sum(e[len(cases)].elapsed_time(e[len(cases) + 1]) for e in evs) / 1e3
     total = t_start.elapsed_time(t_end) / 1e3
-    tp, td, total = max_over_ranks([tp, td, total], dist, dev)
-    launches = K_ * ((1 if do_prefill else 0) + ((1 + (nsplit > 1)) if do_decode else 0))
+    reduced = max_over_ranks(per_case + [td, total], dist, dev)
+    per_case, td, total = reduced[:len(cases)], reduced[-2], reduced[-1]
+    launches = K_ * (len(cases) + (((1 + (nsplit > 1)) if do_decode else 0)))
 
     # ---------------- end to end: pinned host buffers, copies inside the timed region
     # Every step copies its inputs from pinned host memory and reads its result
@@ -429,19 +527,20 @@ def run_ours(args, rank, world, dist):
         return t0.elapsed_time(t1) / 1e3
 
     e2e = None
+    head = cases[0] if cases else None
     if not args.no_e2e:
         E = min(K_, args.e2e_steps)
         h2d = d2h = 0
         ep = ed = 0.0
-        if do_prefill:
+        if head is not None:
             hQ, hK, hV = (torch.from_numpy(t.bits.view(np.int16)).pin_memory()
-                          for t in (xp.Q, xp.K, xp.V))
-            hO = torch.empty(Q.shape, dtype=torch.int16).pin_memory()
-            hL = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
+                          for t in (head.x.Q, head.x.K, head.x.V))
+            hO = torch.empty(head.Q.shape, dtype=torch.int16).pin_memory()
+            hL = torch.empty(head.LSE.shape, dtype=torch.float32).pin_memory()
             h2d += 3 * hQ.numel() * 2
             d2h += hO.numel() * 2 + hL.numel() * 4
-            pb = [(Q, K, V, O, LSE),
-                  tuple(torch.empty_like(t) for t in (Q, K, V, O, LSE))]
+            pb = [(head.Q, head.K, head.V, head.O, head.LSE),
+                  tuple(torch.empty_like(t) for t in (head.Q, head.K, head.V, head.O, head.LSE))]
 
             def p_in(b):
                 for dst, src in zip(pb[b][:3], (hQ, hK, hV)):
@@ -449,10 +548,7 @@ def run_ours(args, rank, world, dist):
 
             def p_cmp(b):
                 q_, k_, v_, o_, l_ = pb[b]
-                if varlen:
-                    fwd(q_, k_, v_, KL, O=o_, LSE=l_, scale=xp.scale, causal=True, stream=stream)
-                else:
-                    fwd(q_, k_, v_, O=o_, LSE=l_, scale=xp.scale, causal=True, stream=stream)
+                head(stream, O=o_, LSE=l_, Q=q_, K=k_, V=v_)
 
             def p_out(b):
                 hO.copy_(pb[b][3].view(torch.int16), non_blocking=True)
@@ -486,9 +582,10 @@ def run_ours(args, rank, world, dist):
             ed = pipelined(E, d_in, d_cmp, d_out)
             del db
         ep, ed = max_over_ranks([ep, ed], dist, dev)
-        e2e = {"value": (whole_job_rate(world, E * flops, ep) / 1e12) if do_prefill else None,
+        e2e = {"value": (whole_job_rate(world, E * head.flops, ep) / 1e12) if head else None,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": E,
+               "workload": head.workload if head else None,
                "decode_gbs": (whole_job_rate(world, E * dbytes, ed) / 1e9) if do_decode else None,
                "path": "pinned host -> cudaMemcpyAsync (copy-in stream) -> C-ABI call (compute "
                        "stream) -> cudaMemcpyAsync (read-back stream) -> pinned host; two "
@@ -498,49 +595,61 @@ def run_ours(args, rank, world, dist):
     if rank != 0:
         return 0
 
+    def prefill_roofline(c, t):
+        per_launch_s = t / K_
+        achieved = c.flops / per_launch_s / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": traffic_for(c.kernel_family, c.workload, c.causal),
+                "peak_source": f"bf16_tflops (burst), of {peak_src}",
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "kernel": c.kernel, "us_per_launch": 1e6 * per_launch_s,
+                **launch_percentiles([e[cases.index(c)].elapsed_time(e[cases.index(c) + 1])
+                                      for e in evs])}
+
     line = {"impl": "ours", "metric": METRIC}
-    cfg = {"workload": args.prefill_workload if do_prefill else args.decode_workload,
-           "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
-    if do_prefill:
-        value = whole_job_rate(world, K_ * flops, tp) / 1e12
-        per_launch_s = tp / K_
-        achieved = flops / per_launch_s / 1e12
-        line.update({"value": value, "unit": "TFLOP/s"})
-        cfg.update({"prefill": {"B": xp.B, "H": xp.H, "S": xp.S, "D": xp.D, "causal": True,
-                                "qk_std": wp["qk_std"], "flops_per_step": flops}})
-        if varlen:
-            # flops count each row's valid keys: min(i + 1, L_b)
-            cfg["prefill"]["key_lens"] = [int(v) for v in xp.key_lens]
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "traffic": traffic_for("prefill_" + pdt, args.prefill_workload),
-                    "peak_source": f"bf16_tflops (burst), of {peak_src}",
-                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "kernel": f"prefill_{pdt}{'_varlen' if varlen else ''}_kernel<{xp.D}, causal>", "us_per_launch": 1e6 * per_launch_s,
-                    **launch_percentiles([e[0].elapsed_time(e[1]) for e in evs])}
-        line["roofline"] = roofline
+    cfg = {"workload": head.workload if head else args.decode_workload,
+           "l2": "inputs larger than L2 (no flush); the S=2048 inputs (50 MB) follow a launch "
+                 "that streams more than L2",
+           "parallelism": f"replicas x{world}"}
+    if head is not None:
+        line.update({"value": whole_job_rate(world, K_ * head.flops, per_case[0]) / 1e12,
+                     "unit": "TFLOP/s"})
+        cfg["prefill"] = head.config()
+        line["roofline"] = prefill_roofline(head, per_case[0])
+        for c, t in zip(cases[1:], per_case[1:]):
+            line[c.key] = {"value": whole_job_rate(world, K_ * c.flops, t) / 1e12,
+                           "unit": "TFLOP/s", "config": c.config(),
+                           "roofline": prefill_roofline(c, t)}
     if do_decode:
         gbs = whole_job_rate(world, K_ * dbytes, td) / 1e9
-        cfg.update({"decode": {"B": xd.B, "H": xd.H, "D": xd.D, "len_range": [512, 8192],
-                               "total_tokens": int(xd.seqlens.sum()), "splits": nsplit,
-                               "bytes_per_step": dbytes}})
+        cfg["decode"] = {"workload": args.decode_workload, "B": xd.B, "H": xd.H, "D": xd.D,
+                         "len_range": [wd["len_lo"], wd["len_hi"]],
+                         "total_tokens": int(xd.seqlens.sum()), "splits": nsplit,
+                         "bytes_per_step": dbytes}
         line["decode"] = {"value": gbs, "unit": "GB/s", "bound": "hbm",
                           "achieved": dbytes / (td / K_) / 1e9, "peak": peaks["hbm_gbs"],
                           "frac": dbytes / (td / K_) / 1e9 / peaks["hbm_gbs"],
-                          "traffic": traffic_for("decode", args.decode_workload), "peak_source": f"hbm_gbs, of {peak_src}",
+                          "traffic": traffic_for("decode", args.decode_workload),
+                          "peak_source": f"hbm_gbs, of {peak_src}",
                           "us_per_call": 1e6 * td / K_,
-                          **launch_percentiles([e[1].elapsed_time(e[2]) for e in evs])}
-        if not do_prefill:
+                          **launch_percentiles([e[len(cases)].elapsed_time(e[len(cases) + 1])
+                                                for e in evs])}
+        if head is None:
             line.update({"value": gbs, "unit": "GB/s"})
+    if clocks is not None and clocks.get("sm_mhz"):
+        clocks["soak_steps"] = soak_steps
+        clocks["ms_per_step_x_sm_mhz"] = 1e3 * total / K_ * clocks["sm_mhz"]
     line.update({
         "n_gpus": world, "steps": K_, "warmup": args.warmup, "ms_per_step": 1e3 * total / K_,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": pdt if do_prefill else ddt,
+        "dtype": head.dtype if head else ddt,
         "data": "synthetic", "config": cfg, "clocks": clocks, "e2e": e2e,
         "gpu_launches": launches,
     })
-    if not args.no_cpu_baseline and world == 1 and do_prefill:
-        line["cpu_baseline"] = oracle_sample_tflops(xp, args.cpu_seconds, workload=args.prefill_workload)
+    if not args.no_cpu_baseline and world == 1 and head is not None:
+        line["cpu_baseline"] = oracle_sample_tflops(head.x, args.cpu_seconds, causal=head.causal,
+                                                    workload=head.workload)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -656,9 +765,57 @@ def run_projections(args, rank, world, dist):
     return 0
 
 
+def free_port():
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def launch_ranks(n):
+    """Run this script as n ranks on this node (one process per GPU), the way
+    torch.distributed.run starts them; returns the launcher's exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def run_dry(args, rank, world):
+    """--dry-run: the multi-rank host path without any CUDA call.  Every rank
+    builds its own seeded batch of the headline prefill recipe (a small slice),
+    joins a gloo group, and the timing reduction runs over dummy times; rank 0
+    prints each rank's seed and input digest."""
+    import torch
+    import torch.distributed as tdist
+    dist = None
+    if world > 1:
+        tdist.init_process_group("gloo")
+        dist = tdist
+    try:
+        w = si.WORKLOADS[PREFILL_WORKLOAD]
+        seed = rank_seed(w["seed"], rank)
+        x = si.prefill_inputs(1, 1, 64, w["D"], seed, qk_std=w["qk_std"])
+        digest = hashlib.sha256(x.Q.bits.tobytes()).hexdigest()
+        ranks = [None] * world
+        if dist is not None:
+            dist.all_gather_object(ranks, {"rank": rank, "seed": seed, "q_sha256": digest})
+        else:
+            ranks = [{"rank": rank, "seed": seed, "q_sha256": digest}]
+        t = max_over_ranks([1.0 + rank], dist, torch.device("cpu"))[0]
+        if rank == 0:
+            print(json.dumps({"dry_run": True, "n_gpus": world, "ranks": ranks,
+                              "max_time_over_ranks": t}), flush=True)
+        return 0
+    finally:
+        if dist is not None:
+            tdist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="ranks (one GPU each); without a launcher, N > 1 starts them itself")
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
@@ -667,7 +824,10 @@ def main():
     ap.add_argument("--prefill-workload", default=PREFILL_WORKLOAD,
                     choices=[k for k, w in si.WORKLOADS.items()
                              if w["kind"] == "prefill" and w["dtype"] in ("bf16", "f16")],
-                    help="prefill workload of the step, bf16 or f16 (default: the headline one)")
+                    help="prefill workload (default: every configuration of the step, the "
+                         "headline first; a workload named here runs alone)")
+    ap.add_argument("--noncausal", action="store_true",
+                    help="with --only prefill: the named workload with causal=0")
     ap.add_argument("--decode-workload", default=DECODE_WORKLOAD,
                     choices=[k for k, w in si.WORKLOADS.items() if w["kind"] == "decode"],
                     help="decode workload of the step (bf16 or f16)")
@@ -675,13 +835,26 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of back-to-back steps before the timed region, sampled "
+                         "with the clocks")
     ap.add_argument("--profile", action="store_true", help="no clock sampling (for ncu runs)")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="the multi-rank host path only (seeds, reduction), no CUDA")
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return launch_ranks(args.gpus)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match WORLD_SIZE={world}")
+    if args.dry_run:
+        return run_dry(args, rank, world)
     dist = None
     if args.impl == "reference":
         return run_reference(args, rank, world)

@@ -91,3 +91,33 @@ def test_launch_percentiles_nearest_rank():
     assert p["us_p95"] == pytest.approx(300.0)
     one = bench.launch_percentiles([0.5])
     assert one == {"us_p50": 500.0, "us_p95": 500.0}
+
+
+def test_bench_gpus_2_starts_two_ranks_itself():
+    """`bench.py --gpus 2` with no launcher in the environment starts two ranks
+    (torch.distributed.run on 127.0.0.1); --dry-run stops before any CUDA call.
+    Each rank reports its own seed and input digest, and the timing reduction
+    is the maximum over both ranks."""
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["dry_run"] is True and d["n_gpus"] == 2
+    ranks = sorted(d["ranks"], key=lambda x: x["rank"])
+    assert [x["rank"] for x in ranks] == [0, 1]
+    assert ranks[0]["seed"] != ranks[1]["seed"]
+    assert ranks[0]["q_sha256"] != ranks[1]["q_sha256"]
+    assert d["max_time_over_ranks"] == 2.0
+
+
+def test_bench_gpus_must_match_the_launcher():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run"],
+                       capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
+    assert r.returncode != 0 and "does not match WORLD_SIZE" in r.stderr
