@@ -27,9 +27,9 @@
 // 128 x 64 slice of A (K-major, 16 KB) and a 64 x 128 slice of W (MN-major:
 // two 64-column blocks of 8 KB), both 128-byte swizzled; both CTAs' copies
 // of a stage complete on the even CTA's barrier.  A persistent grid of
-// pairs walks the tiles in groups of 8 row tiles, all column tiles of a
-// group before the next, so a W slice is reused by the group while it is in
-// L2.  Roles in each CTA:
+// pairs walks the tiles in groups of row tiles sized to L2, all column
+// tiles of a group before the next, so the group's rows of A stay in L2 while
+// W streams through once per group.  Roles in each CTA:
 //   warp 0       TMA producer of its half of the ring
 //   warp 1       tensor-memory allocation (both CTAs together); in the even
 //                CTA one thread issues every MMA and its commits, which
@@ -53,7 +53,6 @@ namespace {
 
 constexpr int GM = 128, GN = 256, GK = 64;     // GM rows per CTA, 2 * GM per pair
 constexpr int kStages = 6;
-constexpr int kGroupM = 8;                     // pair row tiles per scheduling group
 constexpr int A_BYTES = GM * GK * 2;           // 16 KB
 constexpr int B_BLOCK = GK * 64 * 2;           // one 64-column block of W: 8 KB
 constexpr int B_BYTES = 2 * B_BLOCK;           // this CTA's 128 columns: 16 KB
@@ -166,15 +165,18 @@ __device__ __forceinline__ void st_global_v4_g(void* p, uint32_t a, uint32_t b, 
                : "memory");
 }
 
-// Pair tile t -> (row tile of 256 rows, column tile): groups of kGroupM row
-// tiles, column tiles outer within a group.
+// Pair tile t -> (row tile of 256 rows, column tile): groups of group_m row
+// tiles, column tiles outer within a group.  All column tiles of a group
+// reuse its rows of A, so W is read from DRAM about once per group: the host
+// sizes a group to a quarter of L2's worth of A (W's bytes per launch fall
+// with the group count while A is still read about once).
 struct TileMap {
-  int tiles_m, tiles_n;
+  int tiles_m, tiles_n, group_m;
   __device__ void get(int t, int& mt, int& nt) const {
-    const int per_group = kGroupM * tiles_n;
+    const int per_group = group_m * tiles_n;
     const int g = t / per_group, r = t % per_group;
-    const int first = g * kGroupM;
-    const int rows = min(kGroupM, tiles_m - first);
+    const int first = g * group_m;
+    const int rows = min(group_m, tiles_m - first);
     mt = first + r % rows;
     nt = r / rows;
   }
@@ -189,7 +191,7 @@ template <int MODE>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmW,
                                           uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko,
                                           uint16_t* __restrict__ Vo, int tiles_m, int M, int N,
-                                          int Kd, int S, int H, int D, int sblocks,
+                                          int Kd, int S, int H, int D, int sblocks, int group_m,
                                           uint64_t wait_limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -226,7 +228,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{wait_limit_ns, &g_err_gemm_bf16, abort_flag};
-  const TileMap tmap{tiles_m, (N + GN - 1) / GN};
+  const TileMap tmap{tiles_m, (N + GN - 1) / GN, group_m};
   const int ntiles = tmap.tiles_m * tmap.tiles_n;
   const int nk = (Kd + GK - 1) / GK;
   const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
@@ -390,26 +392,27 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     uint16_t* __restrict__ Qo, uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
-                    int M, int N, int Kd, int S, int H, int D, uint64_t wait_limit_ns) {
+                    int M, int N, int Kd, int S, int H, int D, int group_m,
+                    uint64_t wait_limit_ns) {
   gemm_body<MODE_QKV>(tmX, tmW, Qo, Ko, Vo, (M + 2 * GM - 1) / (2 * GM), M, N, Kd, S, H, D, 0,
-                   wait_limit_ns);
+                      group_m, wait_limit_ns);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     out_proj_kernel(const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmW,
-                    uint16_t* __restrict__ Y, int B, int N, int Kd, int S, int D,
+                    uint16_t* __restrict__ Y, int B, int N, int Kd, int S, int D, int group_m,
                     uint64_t wait_limit_ns) {
   const int sblocks = (S + 2 * GM - 1) / (2 * GM);
   gemm_body<MODE_OUT_BHSD>(tmO, tmW, Y, nullptr, nullptr, B * sblocks, 0, N, Kd, S, 0, D,
-                           sblocks, wait_limit_ns);
+                           sblocks, group_m, wait_limit_ns);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     out_proj_rows_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmW, uint16_t* __restrict__ Y, int M,
-                         int N, int Kd, uint64_t wait_limit_ns) {
+                         int N, int Kd, int group_m, uint64_t wait_limit_ns) {
   gemm_body<MODE_OUT_ROWS>(tmA, tmW, Y, nullptr, nullptr, (M + 2 * GM - 1) / (2 * GM), M, N, Kd,
-                           1, 0, 64, 0, wait_limit_ns);
+                           1, 0, 64, 0, group_m, wait_limit_ns);
 }
 
 // ---------------------------------------------------------------- host side
@@ -464,6 +467,32 @@ bool encode_bhsd_4d(CUtensorMap* map, const void* ptr, int B, int H, int S, int 
   return r == CUDA_SUCCESS;
 }
 
+// Row tiles (of 2 * GM rows) per scheduling group: kMinGroupM when all of W
+// (Kd x N bf16) fits in a quarter of L2 and so stays there anyway; else as
+// many as a quarter of L2 holds of their rows of A (K = Kd columns of bf16).
+// The rest of L2 has to hold the W columns and output tiles in flight, and
+// lines read by SMs of both dies; on the Q/K/V product of the LLaMA-7B layer
+// (Kd = 4096: 16 row tiles, 32 MB of A) that measured 1016-1047 MB of DRAM
+// traffic per launch against 1336 MB with groups of 8, while groups of 24 and
+// 32 (48 and 64 MB of A) thrashed (1215 and 2051 MB).
+constexpr int kMinGroupM = 8;
+int group_rows(int Kd, int N, int tiles_m) {
+  static int l2_cached[64] = {0};
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    if (l2_cached[dev] == 0 &&
+        cudaDeviceGetAttribute(&l2_cached[dev], cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      l2_cached[dev] = 0;
+    l2 = l2_cached[dev];
+  }
+  const long long tile_bytes = 2LL * GM * Kd * 2, w_bytes = 2LL * Kd * N;
+  long long g = tile_bytes > 0 ? (static_cast<long long>(l2) / 4 + tile_bytes - 1) / tile_bytes : 0;
+  if (w_bytes <= static_cast<long long>(l2) / 4) g = kMinGroupM;
+  if (g < kMinGroupM) g = kMinGroupM;
+  if (g > tiles_m) g = tiles_m;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
 // Persistent grid of CTA pairs (clusters of 2), as many pairs as can be
 // resident at once, at most one per pair tile.
 template <typename Kern>
@@ -510,14 +539,16 @@ cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H,
     const long long tiles = static_cast<long long>((M + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
     e = launch_pairs(out_proj_rows_kernel, tiles, stream, cfg, attr);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, out_proj_rows_kernel, mo, mw, y, M, N, Kd, wait_limit_ns);
+    const int gm = group_rows(Kd, N, (M + 2 * GM - 1) / (2 * GM));
+    e = cudaLaunchKernelEx(&cfg, out_proj_rows_kernel, mo, mw, y, M, N, Kd, gm, wait_limit_ns);
   } else {
     if (!encode_bhsd_4d(&mo, O, B, H, S, D)) return cudaErrorInvalidValue;
     const long long tiles =
         static_cast<long long>(B) * ((S + 2 * GM - 1) / (2 * GM)) * ((N + GN - 1) / GN);
     e = launch_pairs(out_proj_kernel, tiles, stream, cfg, attr);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, out_proj_kernel, mo, mw, y, B, N, Kd, S, D, wait_limit_ns);
+    const int gm = group_rows(Kd, N, B * ((S + 2 * GM - 1) / (2 * GM)));
+    e = cudaLaunchKernelEx(&cfg, out_proj_kernel, mo, mw, y, B, N, Kd, S, D, gm, wait_limit_ns);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -536,7 +567,9 @@ cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void
   cudaError_t e = launch_pairs(qkv_proj_kernel, tiles, stream, cfg, attr);
   if (e != cudaSuccess) return e;
   uint16_t *q = static_cast<uint16_t*>(Q), *k = static_cast<uint16_t*>(K), *v = static_cast<uint16_t*>(V);
-  e = cudaLaunchKernelEx(&cfg, qkv_proj_kernel, mx, mw, q, k, v, M, N, Kd, S, H, D, wait_limit_ns);
+  const int gm = group_rows(Kd, N, (M + 2 * GM - 1) / (2 * GM));
+  e = cudaLaunchKernelEx(&cfg, qkv_proj_kernel, mx, mw, q, k, v, M, N, Kd, S, H, D, gm,
+                         wait_limit_ns);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
