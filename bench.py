@@ -62,22 +62,28 @@ GEMM_SRC = ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu',
             'causal_head_attention_mha_gb300/csrc/ptx.cuh']
 TRAFFIC = [
     # kernel, workload, causal, sources, sha256 of the sources, bytes per launch
-    ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC, None, None),
-    ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC, None, None),
-    ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC, None, None),
-    ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC, None, None),
-    ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC, None, None),
-    ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC, None, None),
+    ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC,
+     "f064dd9e45962be37d6ed1f8ef379a88e21ed5556599c4964dd2f6ed3d1e8801", 520403968),
+    ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC,
+     "f064dd9e45962be37d6ed1f8ef379a88e21ed5556599c4964dd2f6ed3d1e8801", 529403648),
+    ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC,
+     "f064dd9e45962be37d6ed1f8ef379a88e21ed5556599c4964dd2f6ed3d1e8801", 50637056),
+    ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC,
+     "f064dd9e45962be37d6ed1f8ef379a88e21ed5556599c4964dd2f6ed3d1e8801", 358187520),
+    ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC,
+     "f064dd9e45962be37d6ed1f8ef379a88e21ed5556599c4964dd2f6ed3d1e8801", 526193152),
+    ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC,
+     "f064dd9e45962be37d6ed1f8ef379a88e21ed5556599c4964dd2f6ed3d1e8801", 465210368),
+    # the split kernel's bytes plus the merge kernel's
     ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
-     "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", 1201886720),
-    ("decode", "decode_f16_b16h32d128_len512_8192", True, DECODE_SRC,
-     "4a57a2900bce4d3d7c8d88f0f7cc6c14a2b81669d8e7139e37f15245594dfa2a", 1292623616),
+     "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1202752000),
+    ("decode", "decode_f16_b16h32d128_len512_8192", True, DECODE_SRC, None, None),
     ("qkv_proj", "qkv_bf16_b4s4096hid4096_h32d128", True, GEMM_SRC,
-     "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", 1354212608),
+     "121503fab5ccd8ded0b5056bad7dfec04dadac8327c2730c7dea06a290ca1de1", 1045314048),
     ("out_proj_rows", "outproj_bf16_b4h32s4096d128_n4096", True, GEMM_SRC,
-     "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", 396940544),
+     "121503fab5ccd8ded0b5056bad7dfec04dadac8327c2730c7dea06a290ca1de1", 389191424),
     ("out_proj", "outproj_bf16_b4h32s4096d128_n4096", True, GEMM_SRC,
-     "d4365aeeda8876f4d66ac37b9eb57eae1df6b69289171a103464038b9ac0cc00", 404913152),
+     "121503fab5ccd8ded0b5056bad7dfec04dadac8327c2730c7dea06a290ca1de1", 393275392),
 ]
 
 

@@ -50,9 +50,10 @@ cudaError_t launch_qkv_proj(const void* X, const void* W, void* Q, void* K, void
 cudaError_t launch_out_proj(const void* O, const void* W, void* Y, int B, int H, int S, int D,
                             int n_out, int o_layout, cudaStream_t stream, uint64_t wait_limit_ns);
 
-// Read and clear the device error word of the prefill / projection translation unit.
-cudaError_t take_prefill_bf16_error(unsigned int* word);
-cudaError_t take_gemm_bf16_error(unsigned int* word);
+// Read and clear (one atomic exchange, in order on `stream`, then synchronise
+// it) the device error word of the prefill / projection translation unit.
+cudaError_t take_prefill_bf16_error(unsigned int* word, cudaStream_t stream);
+cudaError_t take_gemm_bf16_error(unsigned int* word, cudaStream_t stream);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();

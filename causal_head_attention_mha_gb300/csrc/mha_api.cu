@@ -244,9 +244,9 @@ int mha_get_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   unsigned int word = 0, word2 = 0;
-  e = mha::take_prefill_bf16_error(&word);
+  e = mha::take_prefill_bf16_error(&word, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
-  e = mha::take_gemm_bf16_error(&word2);
+  e = mha::take_gemm_bf16_error(&word2, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return (word | word2) ? MHA_ERR_TIMEOUT : MHA_OK;
 }

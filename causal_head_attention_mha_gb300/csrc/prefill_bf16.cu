@@ -1088,11 +1088,23 @@ cudaError_t launch_prefill_f16(const void* Q, const void* K, const void* V, void
                               stream, wait_limit_ns, inject);
 }
 
-cudaError_t take_prefill_bf16_error(unsigned int* word) {
-  cudaError_t e = cudaMemcpyFromSymbol(word, g_err_prefill_bf16, sizeof(unsigned int));
+// The error word read and cleared in one atomic step on the device, in
+// stream order on `stream`, so a timeout another launch records meanwhile is
+// either returned here or kept for the next call, never lost between a read
+// and a separate clear.
+__device__ unsigned int g_taken_prefill_bf16 = 0;
+__global__ void status_word_swap_a_kernel() {
+  g_taken_prefill_bf16 = atomicExch(&g_err_prefill_bf16, 0u);
+}
+
+cudaError_t take_prefill_bf16_error(unsigned int* word, cudaStream_t stream) {
+  status_word_swap_a_kernel<<<1, 1, 0, stream>>>();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_err_prefill_bf16, &zero, sizeof(unsigned int));
+  e = cudaMemcpyFromSymbolAsync(word, g_taken_prefill_bf16, sizeof(unsigned int), 0,
+                                cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
 }
 
 }  // namespace mha

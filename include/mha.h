@@ -271,10 +271,12 @@ int mha_out_proj_ex(const void* O, const void* W, void* Y, int B, int H, int S, 
                     int o_layout, void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the device error word that
- * bounded waits set.  Returns MHA_OK, MHA_ERR_TIMEOUT when a wait in some
- * kernel of this library ran out since the last call, or MHA_ERR_CUDA when
- * the synchronisation itself failed.
+ * Synchronises `stream`, then reads and clears the device error words that
+ * bounded waits set (each with one atomic exchange on the device, in order
+ * on `stream`, so a timeout recorded meanwhile by a launch on another stream
+ * is kept for the next call rather than lost).  Returns MHA_OK,
+ * MHA_ERR_TIMEOUT when a wait in some kernel of this library ran out since
+ * the last call, or MHA_ERR_CUDA when the synchronisation itself failed.
  */
 int mha_get_device_status(void* stream);
 
