@@ -26,10 +26,10 @@
 //   warps 4..7   softmax of tile A, one query row per thread (128 keys per
 //                row and tile), P_A,j written as bf16 over the columns of
 //                S_A,j; rescales O_A when the row's reference maximum moves;
-//                item epilogue O_A / l, log-sum-exp.  On f16 data and at
-//                D = 64, P_A,j is handed to the MMA thread in two halves
-//                (keys 0..63, then 64..127), so the product of the first
-//                half with V runs while the second half is computed.
+//                item epilogue O_A / l, log-sum-exp.  At D = 64, P_A,j is
+//                handed to the MMA thread in two halves (keys 0..63, then
+//                64..127), so the product of the first half with V runs
+//                while the second half is computed.
 //   warps 8..11  the same for tile B
 // The issuer orders each key step as P_A,j-1 V_j-1, S_A,j, P_B,j-1 V_j-1,
 // S_B,j: while one tile's softmax runs, the tensor pipe executes the other
@@ -273,8 +273,14 @@ struct Elem<true> {  // f16
   // of the scores within reach on large logits, the f16 path takes every
   // tile's row maximum first and moves the reference only when that maximum
   // passes it by more than kHeadroom: every weight is then <= 2^15 before
-  // any exponential, and no tile is ever redone.
+  // any exponential, and no tile is ever redone.  A move rescales O, which a
+  // warp does for all its rows at once, so when one row must move the warp
+  // moves every row's reference to its tile maximum + kLift (weights <=
+  // 2^-kLift, still f16 normals down to 14 - kLift below the maximum): that
+  // leaves each row kHeadroom + kLift of room before its next move and cut
+  // the warp-tiles with a rescale from 36 % to 5 % on large logits.
   static constexpr float kHeadroom = 15.0f;
+  static constexpr float kLift = 8.0f;
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
   static __device__ __forceinline__ float add_lo(uint32_t w, float a) { return add_f16_lo(w, a); }
   static __device__ __forceinline__ float add_hi(uint32_t w, float a) { return add_f16_hi(w, a); }
@@ -289,10 +295,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
   using C = Cfg<D>;
   using E = Elem<F16>;
   // Hand P_X,j over in two halves (the first half's product with V runs
-  // while the softmax threads compute the second) where that measured
-  // faster: f16 data, and bf16 at D = 64.  bf16 at D = 128 hands the whole
-  // tile over at once (measured 5-7 % faster there).
-  constexpr bool SPLIT = F16 || D == 64;
+  // while the softmax threads compute the second) at D = 64, where that
+  // measured faster.  D = 128 hands the whole tile over at once (measured
+  // 5-7 % faster there for bf16, 3 % for f16).
+  constexpr bool SPLIT = D == 64;
   // valid keys of the sequence of (b, h) = bh: key_lens[b] clamped to [0, S]
   // with key padding (VARLEN), else S
   // element offset of row (bh, q) of O: [B, H, S, D], or [B, S, H, D] when
@@ -497,7 +503,19 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           umma_ss_kmajor_x4(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
         umma_commit(bar(C::B_SFULL + x));
       };
-      while (ok && sch.next(bh, qp)) {
+      // The next item is scheduled one item ahead, while this item's first
+      // products run (with the softmax threads' look-ahead below: measured
+      // 0.8 % faster at D = 64 and 1 % without the causal mask at D = 128,
+      // 1.2 % slower on causal D = 128)
+      constexpr bool AHEAD = (D == 64) || !CAUSAL;
+      int bh_n = 0, qp_n = 0;
+      bool more = AHEAD ? sch.next(bh_n, qp_n) : false;
+      while (ok && (AHEAD ? more : sch.next(bh, qp))) {
+        bool fetched = false;
+        if constexpr (AHEAD) {
+          bh = bh_n;
+          qp = qp_n;
+        }
         const ItemShape sh(qp, S, key_len(bh), CAUSAL);
         const int nx[2] = {sh.nA, sh.nB};
         for (int x = 0; ok && x < 2; ++x)
@@ -550,6 +568,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           }
           // ---- general step (item start and end, ragged tiles)
           const bool s_step = j < sh.nkv, pv_step = j >= 1;
+          if (AHEAD && j == 1) {
+            more = sch.next(bh_n, qp_n);
+            fetched = true;
+          }
           ring.step(pv_step, s_step);
           // Operand waits, where "P_A,lo ready" does not already cover them (no
           // P_A V at this step); a paired unit was waited for when its K was
@@ -589,6 +611,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
         }
         for (int x = 0; x < 2; ++x)
           if (nx[x] > 0) ph = (ph ^ (0x14u << x)) | (0x40u << x);  // Q_X, O_X parity; item done
+        if (AHEAD && !fetched) more = sch.next(bh_n, qp_n);
       }
       // every MMA issued completes before tensor memory is freed
       umma_commit(bar(C::B_DRAIN));
@@ -645,7 +668,17 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     Sched<D == 64> sch(n_qp, BH, CAUSAL);
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
     bool failed = false;
-    while (!failed && sch.next(bh, qp)) {
+    // Where the MMA thread schedules one item ahead, these threads do too:
+    // the next item is scheduled while this item's last P V runs
+    constexpr bool AHEAD = (D == 64) || !CAUSAL;
+    int bh_n = 0, qp_n = 0;
+    bool more = AHEAD ? sch.next(bh_n, qp_n) : false;
+    while (!failed && (AHEAD ? more : sch.next(bh, qp))) {
+      if constexpr (AHEAD) {
+        bh = bh_n;
+        qp = qp_n;
+        more = false;
+      }
       const int L = key_len(bh);
       const ItemShape sh(qp, S, L, CAUSAL);
       const int nx = x ? sh.nB : sh.nA;
@@ -659,6 +692,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           for (int c = 0; c < D; c += 8) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
           if (lse != nullptr) lse[static_cast<size_t>(bh) * S + q] = -INFINITY;
         }
+        if constexpr (AHEAD) more = sch.next(bh_n, qp_n);
         continue;
       }
       float m_run = -INFINITY;  // reference maximum, log2 units
@@ -714,10 +748,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           const bool first = (j == 0);
           float m_use = first ? row_max(s, 0, 8) : m_run;
           if constexpr (F16) {
-            if (!first) {
-              const float mx = row_max(s, 0, 8);
-              if (mx > m_run + E::kHeadroom) m_use = mx;
-            }
+            // the warp's rows move together, each to its tile maximum + kLift
+            const float mx = first ? m_use : row_max(s, 0, 8);
+            if (first)
+              m_use = mx + E::kLift;
+            else if (__any_sync(0xffffffffu, mx > m_run + E::kHeadroom))
+              m_use = fmaxf(m_run, mx + E::kLift);
           }
           const float2 c2 = make_float2(c_log2, c_log2);
           // P_X,j for keys 64h .. 64h + 63 (packed pairs) and its partial sums:
@@ -843,19 +879,22 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           const bool first = (j == 0);
           float m_use = first ? row_max(s) : m_run;
           if constexpr (F16) {
-            if (!first) {
-              const float mx = row_max(s);
-              if (mx > m_run + E::kHeadroom) m_use = mx;
-            }
+            // the warp's rows move together, each to its tile maximum + kLift
+            const float mx = first ? m_use : row_max(s);
+            if (first)
+              m_use = mx + E::kLift;
+            else if (__any_sync(0xffffffffu, mx > m_run + E::kHeadroom))
+              m_use = fmaxf(m_run, mx + E::kLift);
           }
           const float2 c2 = make_float2(c_log2, c_log2);
           // P_X,j and its partial sums: the fp32 weights (for the log-sum-exp and
           // the overflow check) and the bf16-rounded weights the P.V product uses
           // (to normalise O, so that O is an exact convex combination of V rows)
-          uint32_t pk[2][32];
           float rs, rsp;
-#pragma unroll 1
-          for (int pass = 0;; ++pass) {
+          if constexpr (F16) {
+            // f16 never redoes a tile (its reference was set from the tile's
+            // maximum above), so each half of P goes to tensor memory as soon
+            // as it is computed: 32 registers fewer than holding both halves
             const float2 nm2 = make_float2(-m_use, -m_use);
             float2 se[4];
             float sr[8];
@@ -865,34 +904,64 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
             for (int k = 0; k < 8; ++k) sr[k] = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+              uint32_t pk[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const int e0 = 64 * h + 2 * i;
                 const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
                                       c2, nm2);
                 const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
-                pk[h][i] = E::pack(e.x, e.y);
+                pk[i] = E::pack(e.x, e.y);
                 se[i & 3] = add2(se[i & 3], e);
-                if constexpr (!C::ONES) {
-                  sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
-                  sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
-                }
+                sr[(i & 3) * 2] = E::add_lo(pk[i], sr[(i & 3) * 2]);
+                sr[(i & 3) * 2 + 1] = E::add_hi(pk[i], sr[(i & 3) * 2 + 1]);
               }
+              tmem_st_32x32b_x32(tS + 32 * h, pk);
             }
             se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
             rs = se[0].x + se[0].y;
             rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
-            bool redo = false;
-            if constexpr (!F16) redo = pass == 0 && !first && !(rs <= E::kMaxTileWeight);  // also NaN / inf
-            if (!__any_sync(0xffffffffu, redo)) break;
-            // rare: the scores are still in tensor memory (P is stored below)
-            tmem_ld_32x32b_x128(tS, s);
-            if (need_mask) mask(s);
-            if (redo) m_use = fmaxf(m_run, row_max(s));
+          } else {
+            uint32_t pk[2][32];
+#pragma unroll 1
+            for (int pass = 0;; ++pass) {
+              const float2 nm2 = make_float2(-m_use, -m_use);
+              float2 se[4];
+              float sr[8];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) sr[k] = 0.f;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const int e0 = 64 * h + 2 * i;
+                  const float2 v = fma2(make_float2(__uint_as_float(s[e0]), __uint_as_float(s[e0 + 1])),
+                                        c2, nm2);
+                  const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
+                  pk[h][i] = E::pack(e.x, e.y);
+                  se[i & 3] = add2(se[i & 3], e);
+                  if constexpr (!C::ONES) {
+                    sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
+                    sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+                  }
+                }
+              }
+              se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
+              rs = se[0].x + se[0].y;
+              rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+              const bool redo = pass == 0 && !first && !(rs <= E::kMaxTileWeight);  // also NaN / inf
+              if (!__any_sync(0xffffffffu, redo)) break;
+              // rare: the scores are still in tensor memory (P is stored below)
+              tmem_ld_32x32b_x128(tS, s);
+              if (need_mask) mask(s);
+              if (redo) m_use = fmaxf(m_run, row_max(s));
+            }
+            // P_X,j over the first 64 columns of S_X,j, which this thread has read
+            tmem_st_32x32b_x32(tS, pk[0]);
+            tmem_st_32x32b_x32(tS + 32, pk[1]);
           }
-          // P_X,j over the first 64 columns of S_X,j, which this thread has read
-          tmem_st_32x32b_x32(tS, pk[0]);
-          tmem_st_32x32b_x32(tS + 32, pk[1]);
           const bool resc = !first && (m_use != m_run);
           if (__any_sync(0xffffffffu, resc)) {
             // S_X,j complete implies P_X,j-1 V_j-1 complete (issued before it by
@@ -921,6 +990,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       }
       if (failed) break;
       // -------------------------------------------------------- epilogue of the item
+      if constexpr (AHEAD) more = sch.next(bh_n, qp_n);
       failed = !__all_sync(0xffffffffu, mbar_wait(bar(C::B_OFULL + x), no & 1, wc, SITE_SM_OFULL));
       if (failed) break;
       tc_fence_after();
