@@ -889,8 +889,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           const float2 c2 = make_float2(c_log2, c_log2);
           // P_X,j and its partial sums: the fp32 weights (for the log-sum-exp and
           // the overflow check) and the bf16-rounded weights the P.V product uses
-          // (to normalise O, so that O is an exact convex combination of V rows)
-          float rs, rsp;
+          // (to normalise O, so that O is an exact convex combination of V rows;
+          // bf16 takes that second sum after the hand-off, below)
+          float rs, rsp = 0.f;
+          uint32_t pk[2][32];  // bf16: both halves of P, summed after the hand-off
           if constexpr (F16) {
             // f16 never redoes a tile (its reference was set from the tile's
             // maximum above), so each half of P goes to tensor memory as soon
@@ -922,16 +924,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
             rs = se[0].x + se[0].y;
             rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
           } else {
-            uint32_t pk[2][32];
 #pragma unroll 1
             for (int pass = 0;; ++pass) {
               const float2 nm2 = make_float2(-m_use, -m_use);
               float2 se[4];
-              float sr[8];
 #pragma unroll
               for (int k = 0; k < 4; ++k) se[k] = make_float2(0.f, 0.f);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) sr[k] = 0.f;
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -942,15 +940,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
                   const float2 e = make_float2(ex2_approx(v.x), ex2_approx(v.y));
                   pk[h][i] = E::pack(e.x, e.y);
                   se[i & 3] = add2(se[i & 3], e);
-                  if constexpr (!C::ONES) {
-                    sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
-                    sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
-                  }
                 }
               }
               se[0] = add2(add2(se[0], se[1]), add2(se[2], se[3]));
               rs = se[0].x + se[0].y;
-              rsp = ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
               const bool redo = pass == 0 && !first && !(rs <= E::kMaxTileWeight);  // also NaN / inf
               if (!__any_sync(0xffffffffu, redo)) break;
               // rare: the scores are still in tensor memory (P is stored below)
@@ -980,12 +973,27 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           }
           tmem_wait_st();
           l_run += rs;
-          lp_run += rsp;
+          if constexpr (F16) lp_run += rsp;
           m_run = m_use;
           tc_fence_before();
           // failure-detection test mode: the first "P ready" signal of tile A is
           // withheld, so the MMA thread's bounded wait for it runs out
           if (!(inject == 1 && x == 0 && ns == 0)) mbar_arrive(plo);
+          if constexpr (!F16) {
+            // the sum of the rounded weights only normalises O in the epilogue,
+            // so it is taken after P is handed over, off the chain S -> P -> P V
+            float sr[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sr[k] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                sr[(i & 3) * 2] = E::add_lo(pk[h][i], sr[(i & 3) * 2]);
+                sr[(i & 3) * 2 + 1] = E::add_hi(pk[h][i], sr[(i & 3) * 2 + 1]);
+              }
+            lp_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+          }
         }
       }
       if (failed) break;
