@@ -63,17 +63,17 @@ GEMM_SRC = ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu',
 TRAFFIC = [
     # kernel, workload, causal, sources, sha256 of the sources, bytes per launch
     ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC,
-     "b5d7c8d6bdca82aed23a83e41d63abe7b37e2cae6afa4ba16139722ac68eca44", 522155264),
+     "e0f1e4d8710b9f5d825b0dcc67a7404913e441d353aea51eb7ec94cd33440de0", 521670656),
     ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC,
-     "b5d7c8d6bdca82aed23a83e41d63abe7b37e2cae6afa4ba16139722ac68eca44", 529012480),
+     "e0f1e4d8710b9f5d825b0dcc67a7404913e441d353aea51eb7ec94cd33440de0", 529687808),
     ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC,
-     "b5d7c8d6bdca82aed23a83e41d63abe7b37e2cae6afa4ba16139722ac68eca44", 50637568),
+     "e0f1e4d8710b9f5d825b0dcc67a7404913e441d353aea51eb7ec94cd33440de0", 50635776),
     ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC,
-     "b5d7c8d6bdca82aed23a83e41d63abe7b37e2cae6afa4ba16139722ac68eca44", 359384320),
+     "e0f1e4d8710b9f5d825b0dcc67a7404913e441d353aea51eb7ec94cd33440de0", 359716096),
     ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC,
-     "b5d7c8d6bdca82aed23a83e41d63abe7b37e2cae6afa4ba16139722ac68eca44", 520807424),
+     "e0f1e4d8710b9f5d825b0dcc67a7404913e441d353aea51eb7ec94cd33440de0", 521536768),
     ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC,
-     "b5d7c8d6bdca82aed23a83e41d63abe7b37e2cae6afa4ba16139722ac68eca44", 463618816),
+     "e0f1e4d8710b9f5d825b0dcc67a7404913e441d353aea51eb7ec94cd33440de0", 464058368),
     # the split kernel's bytes plus the merge kernel's
     ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
      "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1202752000),
