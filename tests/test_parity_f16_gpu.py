@@ -97,6 +97,39 @@ def test_f16_prefill_reference_moves(causal, D, factor, which):
                       what=f"f16 {which} x{factor} D{D} causal={causal}")
 
 
+def _f16_tensor(v):
+    bits = si.f16_bits(v)
+    out = si.Tensor(si.f16_to_f32(bits), bits)
+    assert np.array_equal(out.values, v)
+    return out
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_f16_prefill_some_rows_of_a_warp_move(causal, D):
+    """Only a few rows of each 32-row warp see their scores jump past the f16
+    headroom in later key tiles: query feature 0 is 200 on rows 3, 40, 77,
+    131, 170 and 250, and key feature 0 is 0 on keys 0..127 and 1 after, so
+    those rows' scores rise by 200 * scale * log2(e) (25 to 36, log2 units)
+    while every other row's change is below 1.  The rows that must move take
+    their warp along (each row to its own tile maximum + 8): the moving rows
+    and the rows moved with them must both match the oracle."""
+    S = 300
+    x = si.prefill_inputs(1, 2, S, D, seed=2711 + D, dtype="f16")
+    q = x.Q.values.copy()
+    k = x.K.values.copy()
+    rows = [3, 40, 77, 131, 170, 250]
+    q[:, :, rows, 0] = 200.0
+    k[:, :, :128, 0] = 0.0
+    k[:, :, 128:, 0] = 1.0
+    Q, K = _f16_tensor(q), _f16_tensor(k)
+    O, L = mha().mha_fwd_f16(dev_tensor(Q, F16), dev_tensor(K, F16), dev_tensor(x.V, F16),
+                             scale=x.scale, causal=causal)
+    Or, Lr = oracle.attention(Q.values, K.values, x.V.values, x.scale, causal)
+    assert_bf16_close(O.float().cpu().numpy(), Or, L.cpu().numpy(), Lr,
+                      what=f"f16 some rows move D{D} causal={causal}")
+
+
 def test_f16_prefill_deterministic():
     x = si.prefill_inputs(2, 4, 1000, 128, seed=41337, dtype="f16")
     Q, K, V = (dev_tensor(t, F16) for t in (x.Q, x.K, x.V))
