@@ -178,17 +178,20 @@ struct ItemShape {
 // (causal: later query blocks first) and dealt to the CTAs in snake order
 // (0..G-1, then G-1..0, ...), which balances the work of each CTA without
 // any shared counter.  Two group shapes:
-//   WIDE = false (D = 128): about two items per CTA per group, the last
-//     group holding whatever heads are left;
-//   WIDE = true (D = 64): about six items per CTA per group, the heads that
-//     would not fill a last group spread over the others (so every group
-//     deals at least G items), and the snake direction carried on from one
-//     group to the next.  On long causal sequences the first shape leaves a
+//   WIDE = false (D = 128 without key padding): about two items per CTA
+//     per group, the last group holding whatever heads are left;
+//   WIDE = true (D = 64, and key padding): about six items per CTA per
+//     group, the heads that would not fill a last group spread over the
+//     others (so every group deals at least G items), and the snake
+//     direction carried on from one group to the next.  On long causal sequences the first shape leaves a
 //     last group of fewer items than CTAs, all of different sizes, and SMs
 //     idle for ~13 % of a launch.  A group of about k items per CTA keeps
 //     k * G * 256 * D * 4 bytes of K and V in flight whatever S is: ~60 MB
 //     here, ~40 MB for D = 128 with k = 2, where k = 4 (80 MB) measured
-//     slower.
+//     slower.  With key padding an item's work also depends on its
+//     sequence's length, which the small D = 128 groups balance poorly (a
+//     model of the bench's key lengths: the busiest CTA 16 % above the
+//     average, against 9 % with the wide groups; measured 4 % faster).
 template <bool WIDE>
 struct Sched {
   int n_qp, BH, G, c, ng, base_h, extra;
@@ -382,7 +385,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     // first key tiles land while the current item is still running.
     if (lane == 0 && warp == kQWarp) {
       prefetch_tensormap(&tmQ);
-      Sched<D == 64> sch(n_qp, BH, CAUSAL);
+      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
       int bh, qp;
       int nq[2] = {0, 0};  // Q_X copies issued
       bool ok = true;
@@ -409,7 +412,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       const uint32_t full0 = bar(C::B_FULL), empty0 = bar(C::B_EMPTY);
-      Sched<D == 64> sch(n_qp, BH, CAUSAL);
+      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
       int bh, qp, n = 0;
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
@@ -449,7 +452,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, BN, false, F16);
       constexpr uint32_t idesc_o = idesc_f32acc(128, C::ON, true, F16);
-      Sched<D == 64> sch(n_qp, BH, CAUSAL);
+      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
       int bh, qp;
       // phase bits: P_X tiles (bit x), Q_X items (bit 2 + x), O_X items (bit
       // 4 + x), and "tile X has finished an item" (bit 6 + x)
@@ -627,7 +630,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     // the MMA thread checks no ring barrier in those steps.  It arrives for
     // a phase only after the previous phase has completed.
     if (C::WATCH && lane == 0) {
-      Sched<D == 64> sch(n_qp, BH, CAUSAL);
+      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
       RingWalk<C::NUNIT, C::PAIRED> ring;
       int bh, qp;
       uint32_t pa = 0;  // phase parity of "P_A,lo ready"
@@ -665,7 +668,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
     const uint32_t tO = tmem + lane_base + C::TM_O + x * C::O_STRIDE;
     const uint32_t sfull = bar(C::B_SFULL + x), plo = bar(C::B_PLO + x), phi = bar(C::B_PHI + x);
-    Sched<D == 64> sch(n_qp, BH, CAUSAL);
+    Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
     bool failed = false;
     // Where the MMA thread schedules one item ahead, these threads do too:
