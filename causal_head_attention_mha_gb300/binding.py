@@ -69,6 +69,8 @@ def _declare(lib):
     lib.mha_fwd_ex.restype = i
     lib.mha_decode_num_splits.argtypes = [i, i]
     lib.mha_decode_num_splits.restype = i
+    lib.mha_prefill_wide_schedule.argtypes = [i, i, i, i, i, i, i]
+    lib.mha_prefill_wide_schedule.restype = i
     lib.mha_get_device_status.argtypes = [vp]
     lib.mha_get_device_status.restype = i
     lib.mha_status_string.argtypes = [i]
@@ -352,6 +354,16 @@ def mha_decode_num_splits(B: int, H: int) -> int:
     if n <= 0:
         raise MHAError(4, "mha_decode_num_splits")
     return n
+
+
+def mha_prefill_wide_schedule(B: int, H: int, S: int, D: int, causal: bool = True,
+                              key_padding: bool = False, sm_count: int = 0) -> bool:
+    """Whether a prefill of this shape deals its query blocks in the wide groups (host only)."""
+    n = _load().mha_prefill_wide_schedule(int(B), int(H), int(S), int(D), int(bool(causal)),
+                                          int(bool(key_padding)), int(sm_count))
+    if n < 0:
+        raise MHAError(-n, "mha_prefill_wide_schedule")
+    return n == 1
 
 
 def mha_get_device_status(stream=None, device=None) -> int:

@@ -57,6 +57,10 @@ cudaError_t take_gemm_bf16_error(unsigned int* word, cudaStream_t stream);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
+// Whether a prefill launch of this shape walks its items in the wide group
+// shape (see prefill_bf16.cu) on a grid of min(items, sm_count) CTAs.
+bool prefill_wide_schedule(int B, int H, int S, int D, bool causal, bool key_padding,
+                           int sm_count);
 
 // Keeps `e` for mha_last_cuda_error, clears it, and returns MHA_ERR_CUDA.
 int record_cuda_failure(cudaError_t e);

@@ -240,6 +240,14 @@ int mha_decode_num_splits(int B, int H) {
   return mha::decode_num_splits(B, H, nsm);
 }
 
+int mha_prefill_wide_schedule(int B, int H, int S, int D, int causal, int key_padding,
+                              int sm_count) {
+  if (B < 1 || H < 1 || S < 1 || (D != 64 && D != 128)) return -MHA_ERR_INVALID_ARG;
+  if (sm_count <= 0) sm_count = mha::device_sm_count();
+  if (sm_count <= 0) return -MHA_ERR_CUDA;
+  return mha::prefill_wide_schedule(B, H, S, D, causal != 0, key_padding != 0, sm_count) ? 1 : 0;
+}
+
 int mha_get_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);

@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdio>
+#include <mutex>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -155,15 +156,17 @@ struct RingWalk {
 
 // Key-tile counts of one item (query block qp of 256 rows) whose sequence
 // has L valid keys (L = S without key padding; keys j >= L are padding).
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+
 struct ItemShape {
   int nA, nB, nkv;  // key tiles used by tile A, by tile B, loaded
   bool hasB;        // tile B has query rows (it does not lie past S)
-  __device__ ItemShape(int qp, int S, int L, bool causal) {
+  __host__ __device__ ItemShape(int qp, int S, int L, bool causal) {
     const int n_kt = (L + BN - 1) / BN;
     hasB = (qp * 2 + 1) * BM < S;
     if (causal) {
-      nA = min(2 * qp + 1, n_kt);
-      nB = hasB ? min(2 * qp + 2, n_kt) : 0;
+      nA = imin(2 * qp + 1, n_kt);
+      nB = hasB ? imin(2 * qp + 2, n_kt) : 0;
     } else {
       nA = n_kt;
       nB = hasB ? n_kt : 0;
@@ -173,36 +176,44 @@ struct ItemShape {
 };
 
 // Static schedule of the work items over a persistent grid, walked
-// identically by every role of a CTA.  Heads are taken in groups whose K and
+// identically by every role of a CTA (and by the host's load model, which
+// picks the group shape per launch).  Heads are taken in groups whose K and
 // V stay in L2; inside a group the items are ranked by decreasing work
 // (causal: later query blocks first) and dealt to the CTAs in snake order
 // (0..G-1, then G-1..0, ...), which balances the work of each CTA without
 // any shared counter.  Two group shapes:
-//   WIDE = false (D = 128 without key padding): about two items per CTA
-//     per group, the last group holding whatever heads are left;
-//   WIDE = true (D = 64, and key padding): about six items per CTA per
-//     group, the heads that would not fill a last group spread over the
-//     others (so every group deals at least G items), and the snake
-//     direction carried on from one group to the next.  On long causal sequences the first shape leaves a
+//   narrow: about two items per CTA per group, the last group holding
+//     whatever heads are left;
+//   wide: about six items per CTA per group, the heads that would not fill
+//     a last group spread over the others (so every group deals at least G
+//     items), and the snake direction carried on from one group to the
+//     next.  On long causal sequences the first shape leaves a
 //     last group of fewer items than CTAs, all of different sizes, and SMs
 //     idle for ~13 % of a launch.  A group of about k items per CTA keeps
 //     k * G * 256 * D * 4 bytes of K and V in flight whatever S is: ~60 MB
 //     here, ~40 MB for D = 128 with k = 2, where k = 4 (80 MB) measured
-//     slower.  With key padding an item's work also depends on its
-//     sequence's length, which the small D = 128 groups balance poorly (a
-//     model of the bench's key lengths: the busiest CTA 16 % above the
-//     average, against 9 % with the wide groups; measured 4 % faster).
-template <bool WIDE>
+//     slower.  D = 64 and key padding always take the wide shape (with key
+//     padding an item's work also depends on its sequence's length, which
+//     the narrow groups balance poorly: on the bench's key lengths a model
+//     puts the busiest CTA 16 % above the average, against 9 % wide;
+//     measured 4 % faster).  D = 128 takes the narrow shape unless a model
+//     of the item costs puts its busiest CTA 5 % or more further above the
+//     average than the wide shape's (see wide_schedule()): measured 6 %
+//     faster narrow on B4 H32 S4096, causal or not, and 10-38 % faster wide
+//     on B2 H16 S16384 (causal and not) and B1 H32 S8192 (not causal).  The
+//     shape is a template parameter of the kernels (both are compiled at
+//     D = 128 and the launch picks one): passed as a kernel argument instead
+//     it measured up to 6 % slower.
 struct Sched {
   int n_qp, BH, G, c, ng, base_h, extra;
-  bool causal;
-  int group, t, rounds;  // rounds dealt in earlier groups (WIDE)
-  __device__ Sched(int n_qp_, int BH_, bool causal_)
-      : n_qp(n_qp_), BH(BH_), G(gridDim.x), c(blockIdx.x), causal(causal_), group(0), t(0),
+  bool causal, wide;
+  int group, t, rounds;  // rounds dealt in earlier groups (wide)
+  __host__ __device__ Sched(int n_qp_, int BH_, bool causal_, bool wide_, int G_, int c_)
+      : n_qp(n_qp_), BH(BH_), G(G_), c(c_), causal(causal_), wide(wide_), group(0), t(0),
         rounds(0) {
-    int target = ((WIDE ? 6 : 2) * G + n_qp - 1) / n_qp;  // heads per group
+    int target = ((wide ? 6 : 2) * G + n_qp - 1) / n_qp;  // heads per group
     if (target < 1) target = 1;
-    if (WIDE) {
+    if (wide) {
       ng = BH / target;
       if (ng < 1) ng = 1;
       base_h = BH / ng;
@@ -213,11 +224,11 @@ struct Sched {
       extra = 0;
     }
   }
-  __device__ bool next(int& bh, int& qp) {
+  __host__ __device__ bool next(int& bh, int& qp) {
     while (true) {
       if (group >= ng) return false;
-      const int h0 = group * base_h + min(group, extra);
-      const int nh = min(base_h + (group < extra ? 1 : 0), BH - h0);
+      const int h0 = group * base_h + imin(group, extra);
+      const int nh = imin(base_h + (group < extra ? 1 : 0), BH - h0);
       const int n = nh * n_qp;
       const int base = t * G;
       if (base >= n) {
@@ -226,7 +237,7 @@ struct Sched {
         t = 0;
         continue;
       }
-      const int dir = (WIDE ? rounds + t : t) & 1;
+      const int dir = (wide ? rounds + t : t) & 1;
       const int r = base + (dir ? (G - 1 - c) : c);
       ++t;
       if (r >= n) continue;
@@ -289,7 +300,7 @@ struct Elem<true> {  // f16
   static __device__ __forceinline__ float add_hi(uint32_t w, float a) { return add_f16_hi(w, a); }
 };
 
-template <int D, bool CAUSAL, bool F16, bool VARLEN>
+template <int D, bool CAUSAL, bool F16, bool VARLEN, bool WIDE>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                              const CUtensorMap& tmV, uint16_t* __restrict__ O,
                                              float* __restrict__ lse, int S, int BH, float c_log2,
@@ -385,7 +396,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     // first key tiles land while the current item is still running.
     if (lane == 0 && warp == kQWarp) {
       prefetch_tensormap(&tmQ);
-      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
+      Sched sch(n_qp, BH, CAUSAL, WIDE, gridDim.x, blockIdx.x);
       int bh, qp;
       int nq[2] = {0, 0};  // Q_X copies issued
       bool ok = true;
@@ -412,7 +423,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       const uint32_t full0 = bar(C::B_FULL), empty0 = bar(C::B_EMPTY);
-      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
+      Sched sch(n_qp, BH, CAUSAL, WIDE, gridDim.x, blockIdx.x);
       int bh, qp, n = 0;
       bool ok = true;
       while (ok && sch.next(bh, qp)) {
@@ -452,7 +463,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f32acc(128, BN, false, F16);
       constexpr uint32_t idesc_o = idesc_f32acc(128, C::ON, true, F16);
-      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
+      Sched sch(n_qp, BH, CAUSAL, WIDE, gridDim.x, blockIdx.x);
       int bh, qp;
       // phase bits: P_X tiles (bit x), Q_X items (bit 2 + x), O_X items (bit
       // 4 + x), and "tile X has finished an item" (bit 6 + x)
@@ -630,7 +641,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     // the MMA thread checks no ring barrier in those steps.  It arrives for
     // a phase only after the previous phase has completed.
     if (C::WATCH && lane == 0) {
-      Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
+      Sched sch(n_qp, BH, CAUSAL, WIDE, gridDim.x, blockIdx.x);
       RingWalk<C::NUNIT, C::PAIRED> ring;
       int bh, qp;
       uint32_t pa = 0;  // phase parity of "P_A,lo ready"
@@ -668,7 +679,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
     const uint32_t tS = tmem + lane_base + C::TM_S + x * 128;
     const uint32_t tO = tmem + lane_base + C::TM_O + x * C::O_STRIDE;
     const uint32_t sfull = bar(C::B_SFULL + x), plo = bar(C::B_PLO + x), phi = bar(C::B_PHI + x);
-    Sched<D == 64 || VARLEN> sch(n_qp, BH, CAUSAL);
+    Sched sch(n_qp, BH, CAUSAL, WIDE, gridDim.x, blockIdx.x);
     int bh, qp, ns = 0, no = 0;  // S_X tiles consumed, O_X items
     bool failed = false;
     // Where the MMA thread schedules one item ahead, these threads do too:
@@ -1048,15 +1059,15 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
 // The kernels: one per 16-bit input type, with and without key padding, the
 // same body.
 #define MHA_PREFILL_KERNEL(NAME, F16, VARLEN)                                              \
-  template <int D, bool CAUSAL>                                                             \
+  template <int D, bool CAUSAL, bool WIDE>                                                  \
   __global__ void __launch_bounds__(kThreads, 1)                                            \
       NAME(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, \
            const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O,                \
            float* __restrict__ lse, int S, int BH, float c_log2,                             \
            const int* __restrict__ key_lens, int H, int o_bshd, uint64_t wait_limit_ns,      \
            int inject) {                                                                     \
-    prefill_body<D, CAUSAL, F16, VARLEN>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, H,  \
-                                         o_bshd, wait_limit_ns, inject);                    \
+    prefill_body<D, CAUSAL, F16, VARLEN, WIDE>(tmQ, tmK, tmV, O, lse, S, BH, c_log2, key_lens, \
+                                               H, o_bshd, wait_limit_ns, inject);           \
   }
 MHA_PREFILL_KERNEL(prefill_bf16_kernel, false, false)
 MHA_PREFILL_KERNEL(prefill_f16_kernel, true, false)
@@ -1100,14 +1111,59 @@ bool encode_bhsd(CUtensorMap* map, const void* ptr, int BH, int S, int D, bool f
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, bool F16, bool VARLEN>
+// Host model of the schedule: each CTA's load walked with the kernel's own
+// Sched (key tiles of its items plus a fixed cost of two per item, an item's
+// start and end), returned as the busiest CTA's load over the average.
+double sched_imbalance(int n_qp, int BH, int S, bool causal, int G, bool wide) {
+  long long total = 0, most = 0;
+  for (int c = 0; c < G; ++c) {
+    Sched sch(n_qp, BH, causal, wide, G, c);
+    long long load = 0;
+    int bh, qp;
+    while (sch.next(bh, qp)) {
+      const ItemShape sh(qp, S, S, causal);
+      load += sh.nA + sh.nB + 2;
+    }
+    total += load;
+    if (load > most) most = load;
+  }
+  return total > 0 ? static_cast<double>(most) * G / static_cast<double>(total) : 1.0;
+}
+
+// Group shape for a launch without key padding at D = 128: wide when the
+// narrow shape's busiest CTA is modelled 5 % or more further above the
+// average (larger groups keep more K and V in flight, which measured slower
+// where both shapes balance).  Launches of more than 2^18 items take the
+// narrow shape unmodelled (many groups balance either way).  Choices are
+// kept in a small table per (shape, grid).
+bool wide_schedule(int n_qp, int BH, int S, bool causal, int G) {
+  if (static_cast<long long>(n_qp) * BH > (1LL << 18)) return false;
+  struct Entry { int n_qp, BH, S, G; bool causal, wide, used; };
+  static Entry table[16] = {};
+  static int next_slot = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : table)
+      if (e.used && e.n_qp == n_qp && e.BH == BH && e.S == S && e.G == G && e.causal == causal)
+        return e.wide;
+  }
+  const bool wide = sched_imbalance(n_qp, BH, S, causal, G, false) >
+                    sched_imbalance(n_qp, BH, S, causal, G, true) + 0.05;
+  std::lock_guard<std::mutex> lock(mu);
+  table[next_slot] = Entry{n_qp, BH, S, G, causal, wide, true};
+  next_slot = (next_slot + 1) % 16;
+  return wide;
+}
+
+template <int D, bool CAUSAL, bool F16, bool VARLEN, bool WIDE>
 cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                      uint16_t* O, float* lse, int BH, int S, float c_log2, const int* key_lens,
                      int H, int o_bshd, cudaStream_t stream, uint64_t wait_limit_ns,
                      int inject) {
   constexpr int smem = Cfg<D>::SMEM_BYTES;
-  auto kern = VARLEN ? (F16 ? prefill_f16_varlen_kernel<D, CAUSAL> : prefill_bf16_varlen_kernel<D, CAUSAL>)
-                     : (F16 ? prefill_f16_kernel<D, CAUSAL> : prefill_bf16_kernel<D, CAUSAL>);
+  auto kern = VARLEN ? (F16 ? prefill_f16_varlen_kernel<D, CAUSAL, WIDE> : prefill_bf16_varlen_kernel<D, CAUSAL, WIDE>)
+                     : (F16 ? prefill_f16_kernel<D, CAUSAL, WIDE> : prefill_bf16_kernel<D, CAUSAL, WIDE>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // The softmax warpgroups raise their register limit with registers the
@@ -1139,19 +1195,39 @@ cudaError_t launch_prefill(const void* Q, const void* K, const void* V, void* O,
     return cudaErrorInvalidValue;
   const float c_log2 = scale * 1.44269504088896340736f;  // scale * log2(e)
   uint16_t* o = static_cast<uint16_t*>(O);
-#define MHA_LAUNCH(DD, CC, VL) \
-  launch_t<DD, CC, F16, VL>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, o_layout, stream, \
-                            wait_limit_ns, inject)
+#define MHA_LAUNCH(DD, CC, VL, WD) \
+  launch_t<DD, CC, F16, VL, WD>(mq, mk, mv, o, LSE, BH, S, c_log2, key_lens, H, o_layout, stream, \
+                                wait_limit_ns, inject)
+  // D = 64 and key padding always deal the items in the wide groups; plain
+  // D = 128 launches take the group shape the schedule model picks
   if (key_lens != nullptr) {
-    if (D == 128) return causal ? MHA_LAUNCH(128, true, true) : MHA_LAUNCH(128, false, true);
-    return causal ? MHA_LAUNCH(64, true, true) : MHA_LAUNCH(64, false, true);
+    if (D == 128) return causal ? MHA_LAUNCH(128, true, true, true) : MHA_LAUNCH(128, false, true, true);
+    return causal ? MHA_LAUNCH(64, true, true, true) : MHA_LAUNCH(64, false, true, true);
   }
-  if (D == 128) return causal ? MHA_LAUNCH(128, true, false) : MHA_LAUNCH(128, false, false);
-  return causal ? MHA_LAUNCH(64, true, false) : MHA_LAUNCH(64, false, false);
+  if (D == 128) {
+    const int n_qp = (S + 2 * BM - 1) / (2 * BM);
+    const long long items = static_cast<long long>(BH) * n_qp;
+    const int nsm = device_sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
+    const bool wide = wide_schedule(n_qp, BH, S, causal != 0, static_cast<int>(items < nsm ? items : nsm));
+    if (causal) return wide ? MHA_LAUNCH(128, true, false, true) : MHA_LAUNCH(128, true, false, false);
+    return wide ? MHA_LAUNCH(128, false, false, true) : MHA_LAUNCH(128, false, false, false);
+  }
+  return causal ? MHA_LAUNCH(64, true, false, true) : MHA_LAUNCH(64, false, false, true);
 #undef MHA_LAUNCH
 }
 
 }  // namespace
+
+bool prefill_wide_schedule(int B, int H, int S, int D, bool causal, bool key_padding,
+                           int sm_count) {
+  if (D == 64 || key_padding) return true;
+  const int BH = B * H;
+  const int n_qp = (S + 2 * BM - 1) / (2 * BM);
+  const long long items = static_cast<long long>(BH) * n_qp;
+  const int grid = static_cast<int>(items < sm_count ? items : sm_count);
+  return wide_schedule(n_qp, BH, S, causal, grid);
+}
 
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 const int* key_lens, int B, int H, int S, int D, float scale,

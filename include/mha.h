@@ -209,6 +209,22 @@ int mha_decode_noalloc(const void* q, const void* Kcache, const void* Vcache,
 int mha_decode_num_splits(int B, int H);
 
 /*
+ * Which work-item schedule mha_fwd / mha_fwd_f16 (key_padding = 0) or the
+ * _varlen calls (key_padding = 1) use for this shape: 1 = the wide groups
+ * (about six 256-row query blocks per CTA per group of heads), 0 = the
+ * narrow ones (about two).  A persistent grid of min(B*H*ceil(S/256),
+ * sm_count) CTAs deals the query blocks; the choice is made per launch from
+ * a model of each CTA's load (D = 64 and key padding always take the wide
+ * groups).  sm_count <= 0 takes the current device's count.  Host
+ * arithmetic only (no GPU work), except for reading the device's SM count.
+ * Returns 1 or 0, or a negative MHA_ERR_* code: -MHA_ERR_INVALID_ARG for a
+ * non-positive size or D other than 64 and 128, -MHA_ERR_CUDA when the SM
+ * count cannot be read.
+ */
+int mha_prefill_wide_schedule(int B, int H, int S, int D, int causal, int key_padding,
+                              int sm_count);
+
+/*
  * Fused Q, K, V projection feeding the attention calls: page 3 section 2
  * (Q = X W_Q, K = X W_K, V = X W_V) with its section 2.1 shapes, the three
  * products fused into one GEMM as page 1 section 2.1 ("Week 4 CUDA notes")

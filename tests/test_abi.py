@@ -183,3 +183,27 @@ def test_out_proj_ex_validation(lib, kw, expected):
     a.update(kw)
     assert lib.mha_out_proj_ex(a["O"], a["W"], a["Y"], a["B"], a["H"], a["S"], a["D"], a["n_out"],
                                a["o_layout"], None) == expected
+
+
+# The prefill schedule choice (host arithmetic only; sm_count given, so no
+# device is queried).  Each expectation is the group shape that measured
+# faster on a GB300 for that shape.
+@pytest.mark.parametrize("B,H,S,causal,wide", [
+    (4, 32, 4096, 1, 0),    # the bench shape: narrow 6 % faster
+    (4, 32, 4096, 0, 0),    # the same without the causal mask: narrow 6 % faster
+    (2, 16, 16384, 1, 1),   # wide 10 % faster
+    (2, 16, 16384, 0, 1),   # wide 32 % faster
+    (1, 32, 8192, 0, 1),    # wide 38 % faster
+])
+def test_prefill_schedule_choice_d128(lib, B, H, S, causal, wide):
+    assert lib.mha_prefill_wide_schedule(B, H, S, 128, causal, 0, 152) == wide
+
+
+def test_prefill_schedule_choice_fixed_cases_and_errors(lib):
+    # D = 64 and key padding always take the wide groups
+    assert lib.mha_prefill_wide_schedule(4, 32, 4096, 64, 1, 0, 152) == 1
+    assert lib.mha_prefill_wide_schedule(4, 32, 4096, 128, 1, 1, 152) == 1
+    # a single item per CTA or less: both shapes deal the same items
+    assert lib.mha_prefill_wide_schedule(1, 1, 256, 128, 1, 0, 152) in (0, 1)
+    for bad in ((0, 32, 4096, 128), (4, 0, 4096, 128), (4, 32, 0, 128), (4, 32, 4096, 96)):
+        assert lib.mha_prefill_wide_schedule(*bad, 1, 0, 152) == -INVALID
