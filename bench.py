@@ -63,17 +63,17 @@ GEMM_SRC = ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu',
 TRAFFIC = [
     # kernel, workload, causal, sources, sha256 of the sources, bytes per launch
     ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC,
-     "6ec5a874cfee6103c496830627aac8d5aa288b1a2c2142f37b92ccc58d2d415a", 522761728),
+     "4c72e6df91963bd548690b0050147db8e4def9b296ca83e7cae5144d1040d30e", 522761728),
     ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC,
-     "6ec5a874cfee6103c496830627aac8d5aa288b1a2c2142f37b92ccc58d2d415a", 528296960),
+     "4c72e6df91963bd548690b0050147db8e4def9b296ca83e7cae5144d1040d30e", 528296960),
     ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC,
-     "6ec5a874cfee6103c496830627aac8d5aa288b1a2c2142f37b92ccc58d2d415a", 50585088),
+     "4c72e6df91963bd548690b0050147db8e4def9b296ca83e7cae5144d1040d30e", 50585088),
     ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC,
-     "6ec5a874cfee6103c496830627aac8d5aa288b1a2c2142f37b92ccc58d2d415a", 352894208),
+     "4c72e6df91963bd548690b0050147db8e4def9b296ca83e7cae5144d1040d30e", 352894208),
     ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC,
-     "6ec5a874cfee6103c496830627aac8d5aa288b1a2c2142f37b92ccc58d2d415a", 523592960),
+     "4c72e6df91963bd548690b0050147db8e4def9b296ca83e7cae5144d1040d30e", 523592960),
     ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC,
-     "6ec5a874cfee6103c496830627aac8d5aa288b1a2c2142f37b92ccc58d2d415a", 832104448),
+     "4c72e6df91963bd548690b0050147db8e4def9b296ca83e7cae5144d1040d30e", 832104448),
     # the split kernel's bytes plus the merge kernel's
     ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
      "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1202752000),

@@ -154,10 +154,10 @@ struct RingWalk {
   }
 };
 
-// Key-tile counts of one item (query block qp of 256 rows) whose sequence
-// has L valid keys (L = S without key padding; keys j >= L are padding).
 __host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 
+// Key-tile counts of one item (query block qp of 256 rows) whose sequence
+// has L valid keys (L = S without key padding; keys j >= L are padding).
 struct ItemShape {
   int nA, nB, nkv;  // key tiles used by tile A, by tile B, loaded
   bool hasB;        // tile B has query rows (it does not lie past S)
@@ -1056,8 +1056,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
   }
 }
 
-// The kernels: one per 16-bit input type, with and without key padding, the
-// same body.
+// The kernels: one per 16-bit input type, with and without key padding, and
+// per group shape of the item schedule (WIDE), the same body.
 #define MHA_PREFILL_KERNEL(NAME, F16, VARLEN)                                              \
   template <int D, bool CAUSAL, bool WIDE>                                                  \
   __global__ void __launch_bounds__(kThreads, 1)                                            \
