@@ -86,6 +86,23 @@ def test_bf16_prefill_many_items_per_cta(causal, D):
                       what=f"B8 H40 S600 D{D} causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("B,H,S,causal", [(4, 40, 512, True), (4, 32, 768, False)])
+def test_prefill_wide_item_schedule(B, H, S, causal, dtype):
+    """Plain D = 128 shapes whose item schedule takes the wide groups (the
+    host's load model picks them on this GPU), every output compared."""
+    if not mha().mha_prefill_wide_schedule(B, H, S, 128, causal=causal):
+        pytest.skip("the narrow groups are chosen on this GPU's SM count")
+    f16 = dtype == torch.float16
+    x = si.prefill_inputs(B, H, S, 128, seed=7300 + S, dtype="f16" if f16 else "bf16")
+    fwd = mha().mha_fwd_f16 if f16 else mha().mha_fwd
+    O, L = fwd(dev_tensor(x.Q, dtype), dev_tensor(x.K, dtype), dev_tensor(x.V, dtype),
+               scale=x.scale, causal=causal)
+    Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal)
+    assert_bf16_close(O.float().cpu().numpy(), Or, L.cpu().numpy(), Lr,
+                      what=f"wide schedule B{B} H{H} S{S} causal={causal} {dtype}")
+
+
 def _scale_keys(t, lo, hi, factor):
     """K with keys lo..hi-1 multiplied by a power of two (exact in bf16)."""
     v = t.values.copy()
