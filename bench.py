@@ -77,7 +77,8 @@ TRAFFIC = [
     # the split kernel's bytes plus the merge kernel's
     ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
      "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1202752000),
-    ("decode", "decode_f16_b16h32d128_len512_8192", True, DECODE_SRC, None, None),
+    ("decode", "decode_f16_b16h32d128_len512_8192", True, DECODE_SRC,
+     "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1293512192),
     ("qkv_proj", "qkv_bf16_b4s4096hid4096_h32d128", True, GEMM_SRC,
      "121503fab5ccd8ded0b5056bad7dfec04dadac8327c2730c7dea06a290ca1de1", 1045314048),
     ("out_proj_rows", "outproj_bf16_b4h32s4096d128_n4096", True, GEMM_SRC,
