@@ -283,17 +283,17 @@ struct Elem<false> {  // bf16
 template <>
 struct Elem<true> {  // f16
   static constexpr uint32_t kOne = 0x3C00u;  // 1.0
-  // f16 ends at 65504, so weights must stay <= 2^15.  With a 15 (log2) jump
+  // f16 ends at 65504, so weights must stay below it.  With a 16 (log2) jump
   // of the scores within reach on large logits, the f16 path takes every
   // tile's row maximum first and moves the reference only when that maximum
-  // passes it by more than kHeadroom: every weight is then <= 2^15 before
-  // any exponential, and no tile is ever redone.  A move rescales O, which a
+  // passes it by more than kHeadroom: every weight is then <= 2^15.9 (61152
+  // once rounded to f16) before any exponential, and no tile is ever redone.  A move rescales O, which a
   // warp does for all its rows at once, so when one row must move the warp
   // moves every row's reference to its tile maximum + kLift (weights <=
   // 2^-kLift, still f16 normals down to 14 - kLift below the maximum): that
   // leaves each row kHeadroom + kLift of room before its next move and cut
   // the warp-tiles with a rescale from 36 % to 5 % on large logits.
-  static constexpr float kHeadroom = 15.0f;
+  static constexpr float kHeadroom = 15.9f;
   static constexpr float kLift = 8.0f;
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
   static __device__ __forceinline__ float add_lo(uint32_t w, float a) { return add_f16_lo(w, a); }
@@ -759,7 +759,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           // passes the bound (scores above the reference by ~64, log2 units)
           // is redone from its scores with its true maximum, and O is rescaled,
           // before any of its weights are handed over.  (That is the bf16
-          // path; the f16 path, whose weights must stay <= 2^15, takes every
+          // path; the f16 path, whose weights must stay below 65504, takes every
           // tile's row maximum instead: see Elem<true>.)
           const bool first = (j == 0);
           float m_use = first ? row_max(s, 0, 8) : m_run;
@@ -890,7 +890,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           // exact arithmetic.  A tile that does overflow (its scores exceed the
           // reference by ~64, log2 units) is redone from tensor memory with its
           // true maximum, and O is rescaled.  (That is the bf16 path; the f16
-          // path, whose weights must stay <= 2^15, takes every tile's row
+          // path, whose weights must stay below 65504, takes every tile's row
           // maximum instead: see Elem<true>.)
           const bool first = (j == 0);
           float m_use = first ? row_max(s) : m_run;

@@ -4,7 +4,7 @@ The same checks as the bf16 path, on f16 inputs: element by element on small
 shapes (several tiles, ragged tails, several work items per CTA), on sampled
 rows of the full-size f16 bench workload, moves of the reference maximum
 (f16 weights are kept <= 2^15: the f16 kernel takes each tile's row maximum and
-moves the reference, rescaling O, when the scores jump by more than 15 log2
+moves the reference, rescaling O, when the scores jump by more than 15.9 log2
 units), and decode.  The tolerances are
 the bf16 ones (f16 keeps more mantissa bits, so they are looser for it).
 """
@@ -84,7 +84,7 @@ def _scale_keys_f16(t, lo, hi, factor):
 @pytest.mark.parametrize("which", ["later_keys_dominate", "first_keys_dominate"])
 def test_f16_prefill_reference_moves(causal, D, factor, which):
     """Keys scaled by 8 push later scores ~20-30 (log2 units) above an item's
-    first-tile reference, past the f16 headroom of 15: the reference moves and
+    first-tile reference, past the f16 headroom of 15.9: the reference moves and
     O is rescaled; by 64 the jump is larger still, and with the first keys
     scaled the later tiles underflow against the reference."""
     S = 300
