@@ -63,17 +63,17 @@ GEMM_SRC = ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu',
 TRAFFIC = [
     # kernel, workload, causal, sources, sha256 of the sources, bytes per launch
     ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC,
-     "6f76049e2dd7bdb403d379d35a3b004040429d5c6f1ba15cec8c4a178b7adfb9", 522740480),
+     "8a06123d81a268f4933b3dd6570b71a347c8e9967d52d185303198d855012679", 522740480),
     ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC,
-     "6f76049e2dd7bdb403d379d35a3b004040429d5c6f1ba15cec8c4a178b7adfb9", 528795136),
+     "8a06123d81a268f4933b3dd6570b71a347c8e9967d52d185303198d855012679", 528795136),
     ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC,
-     "6f76049e2dd7bdb403d379d35a3b004040429d5c6f1ba15cec8c4a178b7adfb9", 50768384),
+     "8a06123d81a268f4933b3dd6570b71a347c8e9967d52d185303198d855012679", 50768384),
     ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC,
-     "6f76049e2dd7bdb403d379d35a3b004040429d5c6f1ba15cec8c4a178b7adfb9", 357255424),
+     "8a06123d81a268f4933b3dd6570b71a347c8e9967d52d185303198d855012679", 357255424),
     ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC,
-     "6f76049e2dd7bdb403d379d35a3b004040429d5c6f1ba15cec8c4a178b7adfb9", 523040512),
+     "8a06123d81a268f4933b3dd6570b71a347c8e9967d52d185303198d855012679", 521219584),
     ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC,
-     "6f76049e2dd7bdb403d379d35a3b004040429d5c6f1ba15cec8c4a178b7adfb9", 838945024),
+     "8a06123d81a268f4933b3dd6570b71a347c8e9967d52d185303198d855012679", 838945024),
     # the split kernel's bytes plus the merge kernel's
     ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
      "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1202752000),
