@@ -1,4 +1,5 @@
-"""Measured errors of the GPU path against the fp64 oracle on the five workloads.
+"""Measured errors of the GPU path against the fp64 oracle on the five workloads,
+plus the f16 and key-padding prefill workloads of the bench.
 
 Not a test (pytest does not collect it): it prints one markdown row per
 workload with the largest absolute error of O, its relative Frobenius error
@@ -34,6 +35,10 @@ def prefill_row(name, causal, rows_per_bh=None):
     if w["dtype"] == "f32":
         O, L = mha.mha_fwd_f32(dev_tensor(x.Q, torch.float32), dev_tensor(x.K, torch.float32),
                                dev_tensor(x.V, torch.float32), scale=x.scale, causal=causal)
+    elif x.key_lens is not None:
+        kl = torch.from_numpy(np.ascontiguousarray(x.key_lens, dtype=np.int32)).cuda()
+        O, L = mha.mha_fwd_varlen(dev_tensor(x.Q, torch.bfloat16), dev_tensor(x.K, torch.bfloat16),
+                                  dev_tensor(x.V, torch.bfloat16), kl, scale=x.scale, causal=causal)
     else:
         tdt = torch.float16 if w["dtype"] == "f16" else torch.bfloat16
         fn = mha.mha_fwd_f16 if w["dtype"] == "f16" else mha.mha_fwd
@@ -43,11 +48,13 @@ def prefill_row(name, causal, rows_per_bh=None):
     L = L.cpu().numpy().reshape(-1)
     if rows_per_bh is None:
         rows = np.arange(x.B * x.H * x.S)
-        Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal)
+        Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal,
+                                  key_lens=x.key_lens)
         Or, Lr = Or.reshape(-1, x.D), Lr.reshape(-1)
     else:
         rows = sample_rows(x.B, x.H, x.S, 8, rows_per_bh, seed=7)
-        Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows)
+        Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows,
+                                  key_lens=x.key_lens)
     max_abs, frob = errors(O[rows], Or)
     lse = float(np.max(np.abs(L[rows] - Lr)))
     what = "all rows" if rows_per_bh is None else f"{len(rows)} sampled rows"
@@ -78,6 +85,10 @@ def main():
         ("4. decode bf16 B16 H32 D128", lambda: decode_row("decode_bf16_b16h32d128_len512_8192")),
         ("5. bf16 B2 H16 S16384 D64, causal",
          lambda: prefill_row("prefill_bf16_b2h16s16384d64", True, rows_per_bh=256)),
+        ("f16 B4 H32 S4096 D128 qk3, causal",
+         lambda: prefill_row("prefill_f16_b4h32s4096d128_qk3", True, rows_per_bh=192)),
+        ("key padding bf16 B4 H32 S4096 D128, causal",
+         lambda: prefill_row("prefill_varlen_bf16_b4h32s4096d128", True, rows_per_bh=192)),
     ]
     print("| Workload | max-abs | rel-Frobenius | LSE max-abs | compared |")
     print("|---|---:|---:|---:|---|")
