@@ -143,6 +143,7 @@ struct RingWalk {
     if (cur == 2 * NUNIT) cur = 1;
     else if (cur == 2 * NUNIT + 1) cur = 0;
   }
+  __device__ __forceinline__ uint32_t peek() const { return cur; }  // the next take
   __device__ __forceinline__ void step(bool pv_step, bool s_step) {
     if (pv_step) {
       if constexpr (PAIRED)
@@ -508,8 +509,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
           umma_ts_mnmajor_x4(tO, tP, desc(v_lo), idesc_o, acc);
       };
       // S_X = Q_X K_j^T (K-major operands, LBO unused), then S_FULL[X]
-      auto issue_s = [&](int x) {
-        const uint32_t k_lo = ring_lo + (ring.kpos >> 1) * kUnitLo + (1u << 16);
+      auto issue_s = [&](int x, uint32_t kpos) {
+        const uint32_t k_lo = ring_lo + (kpos >> 1) * kUnitLo + (1u << 16);
         const uint32_t tS = tmem + C::TM_S + x * 128;
         if constexpr (D == 128)
           umma_ss_kmajor_x8(tS, desc(q_lo + x * (C::TILE_BYTES >> 4)), desc(k_lo), idesc_s, 0u);
@@ -523,6 +524,17 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       // 1 % and 4 % faster there; on causal D = 128 without key padding
       // this thread's look-ahead measured 1 % slower)
       constexpr bool AHEAD = (D == 64) || !CAUSAL || VARLEN;
+      // Early start: tile A's first S product of the next item is issued in
+      // this item's last step, before the wait for tile B's last weights,
+      // once the next Q_A and K_0 have landed (probed, never waited for), so
+      // tile A's softmax starts the next item while tile B's finishes this
+      // one.  Measured 1-3 % faster on the long sequences that take the wide
+      // groups at D = 128; 0.3-1.9 % slower on the short items of the narrow
+      // groups (the two softmax warpgroups then compete for the exp unit
+      // instead of overlapping with the tensor core), and 3 % slower at
+      // D = 64 (the MMA thread's added state spills).
+      constexpr bool EARLY = (D == 128) && WIDE && !VARLEN;
+      bool early_a = false;  // S_A,0 of this item was issued in the previous one
       int bh_n = 0, qp_n = 0;
       bool more = AHEAD ? sch.next(bh_n, qp_n) : false;
       while (ok && (AHEAD ? more : sch.next(bh, qp))) {
@@ -562,7 +574,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
               tc_fence_after();
             }
             issue_pv(0, 1, 1u);
-            issue_s(0);
+            issue_s(0, ring.kpos);
             ok = mbar_wait(bar(C::B_PLO + 1), bit(1), wc, SITE_MMA_PLO);
             if (!ok) break;
             tc_fence_after();
@@ -575,7 +587,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
             issue_pv(1, 1, 1u);
             // tile B's P V is the last reader of V_j-1 (and, paired, of K_j-1)
             umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.vpos >> 1)));
-            issue_s(1);
+            issue_s(1, ring.kpos);
             // K_j's last reader is S_B,j (unpaired units only)
             if (!C::PAIRED) umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.kpos >> 1)));
             ph ^= 3u;
@@ -597,6 +609,28 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
             if (ok && s_step) ok = mbar_wait(full_bar(ring.kpos), ring.kpos & 1, wc, SITE_MMA_KFULL);
           }
           for (int x = 0; ok && x < 2; ++x) {
+            if constexpr (EARLY) {
+              // the item's last step, after tile A's last P V (S_A,0 of the
+              // next item overwrites P_A) and before tile B's wait; without
+              // key padding every item has tile A, so the next one loads Q_A
+              if (x == 1 && j == sh.nkv) {
+                bool next_item;
+                if constexpr (AHEAD) {
+                  next_item = more;
+                } else {
+                  Sched pk = sch;
+                  int bh2, qp2;
+                  next_item = pk.next(bh2, qp2);
+                }
+                const uint32_t kp = ring.peek();
+                if (next_item && mbar_test_wait(bar(C::B_QFULL), bit(2) ^ 1u) &&
+                    mbar_test_wait(full_bar(kp), kp & 1)) {
+                  tc_fence_after();
+                  issue_s(0, kp);
+                  early_a = true;
+                }
+              }
+            }
             if (pv_step && j - 1 < nx[x]) {
               ok = mbar_wait(bar(C::B_PLO + x), bit(x), wc, SITE_MMA_PLO);
               // O_X was last read by the previous item's epilogue (O_X items
@@ -617,12 +651,19 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
             }
             if (x == 1 && pv_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.vpos >> 1)));
             if (s_step && j < nx[x]) {
-              tc_fence_after();
-              issue_s(x);
+              // (an S_A,0 issued early still releases Q_A only here, after
+              // this item's wait for Q_A: the producer stays within a phase)
+              if (!(EARLY && x == 0 && j == 0 && early_a)) {
+                tc_fence_after();
+                issue_s(x, ring.kpos);
+              }
               if (j == nx[x] - 1) umma_commit(bar(C::B_QEMPTY + x));
             }
           }
           if (!C::PAIRED && ok && s_step) umma_commit(bar(C::B_EMPTY + static_cast<int>(ring.kpos >> 1)));
+          if constexpr (EARLY) {
+            if (j == 0) early_a = false;
+          }
         }
         for (int x = 0; x < 2; ++x)
           if (nx[x] > 0) ph = (ph ^ (0x14u << x)) | (0x40u << x);  // Q_X, O_X parity; item done

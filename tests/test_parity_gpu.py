@@ -185,6 +185,37 @@ def test_bf16_prefill_workload_sampled(name, causal):
     assert torch.isfinite(L).all()
 
 
+# Long D = 128 sequences take the wide item groups, where tile A's first S
+# product of an item is issued in the previous item's last step
+LONG_WIDE = [
+    (2, 16, 16384, True, torch.bfloat16),
+    (2, 16, 16384, False, torch.bfloat16),
+    (1, 32, 8192, False, torch.bfloat16),
+    (2, 16, 16384, True, torch.float16),
+]
+
+
+@pytest.mark.parametrize("B,H,S,causal,dtype", LONG_WIDE)
+def test_prefill_long_wide_sampled(B, H, S, causal, dtype):
+    """Sampled rows (random rows and tile edges of sampled heads, so the first
+    tiles of many items) of long D = 128 prefills against the oracle."""
+    if not mha().mha_prefill_wide_schedule(B, H, S, 128, causal=causal):
+        pytest.skip("the narrow groups are chosen on this GPU's SM count")
+    f16 = dtype == torch.float16
+    x = si.prefill_inputs(B, H, S, 128, seed=8100 + S + int(causal), qk_std=3.0 if f16 else 1.0,
+                          dtype="f16" if f16 else "bf16")
+    Q, K, V = (dev_tensor(t, dtype) for t in (x.Q, x.K, x.V))
+    fwd = mha().mha_fwd_f16 if f16 else mha().mha_fwd
+    O, L = fwd(Q, K, V, scale=x.scale, causal=causal)
+    rows = sample_rows(x.B, x.H, x.S, n_bh=8, rows_per_bh=64, seed=11)
+    Or, Lr = oracle.attention(x.Q.values, x.K.values, x.V.values, x.scale, causal, rows=rows)
+    Og = O.view(-1, x.D)[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    Lg = L.view(-1)[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_bf16_close(Og, Or, Lg, Lr, what=f"B{B} H{H} S{S} causal={causal} {dtype}")
+    assert torch.isfinite(O.float()).all()
+    assert torch.isfinite(L).all()
+
+
 # ------------------------------------------------------------------ decode
 @pytest.mark.parametrize("B,H,D,lens", [
     (3, 4, 128, [1, 200, 77]),
