@@ -531,8 +531,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& tmQ, const CUten
       // one.  Measured 1-3 % faster on the long sequences that take the wide
       // groups at D = 128; 0.3-1.9 % slower on the short items of the narrow
       // groups (the two softmax warpgroups then compete for the exp unit
-      // instead of overlapping with the tensor core), and 3 % slower at
-      // D = 64 (the MMA thread's added state spills).
+      // instead of overlapping with the tensor core), and 2.4-3 % slower at
+      // D = 64.
       constexpr bool EARLY = (D == 128) && WIDE && !VARLEN;
       bool early_a = false;  // S_A,0 of this item was issued in the previous one
       int bh_n = 0, qp_n = 0;
