@@ -87,10 +87,15 @@ def test_bf16_prefill_many_items_per_cta(causal, D):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("B,H,S,causal", [(4, 40, 512, True), (4, 32, 768, False)])
+@pytest.mark.parametrize("B,H,S,causal", [(4, 40, 512, True), (4, 32, 768, False),
+                                           (4, 40, 384, False), (4, 40, 300, False),
+                                           (8, 16, 700, True), (4, 40, 1000, True)])
 def test_prefill_wide_item_schedule(B, H, S, causal, dtype):
     """Plain D = 128 shapes whose item schedule takes the wide groups (the
-    host's load model picks them on this GPU), every output compared."""
+    host's load model picks them on this GPU), every output compared.  There
+    tile A of each item starts while tile B finishes the item before, also
+    after items whose last query block has no tile B (S = 384, 300) and after
+    ragged tiles (S = 300, 700, 1000)."""
     if not mha().mha_prefill_wide_schedule(B, H, S, 128, causal=causal):
         pytest.skip("the narrow groups are chosen on this GPU's SM count")
     f16 = dtype == torch.float16
