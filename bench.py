@@ -63,17 +63,17 @@ GEMM_SRC = ['causal_head_attention_mha_gb300/csrc/gemm_bf16.cu',
 TRAFFIC = [
     # kernel, workload, causal, sources, sha256 of the sources, bytes per launch
     ("prefill_bf16", PREFILL_WORKLOAD, True, PREFILL_SRC,
-     "145be21612b5eca3bbc8749990827d96b04fd454a2ce731779456ce90ce96e3b", 521016832),
+     "4b16b779af583ecbe033acd248a3aa91760027bc0fe100fa345cb03f55d3d09e", 521016832),
     ("prefill_bf16", PREFILL_WORKLOAD, False, PREFILL_SRC,
-     "145be21612b5eca3bbc8749990827d96b04fd454a2ce731779456ce90ce96e3b", 528776192),
+     "4b16b779af583ecbe033acd248a3aa91760027bc0fe100fa345cb03f55d3d09e", 528776192),
     ("prefill_bf16", "prefill_bf16_b1h32s2048d128", True, PREFILL_SRC,
-     "145be21612b5eca3bbc8749990827d96b04fd454a2ce731779456ce90ce96e3b", 50631424),
+     "4b16b779af583ecbe033acd248a3aa91760027bc0fe100fa345cb03f55d3d09e", 50631424),
     ("prefill_bf16", "prefill_bf16_b2h16s16384d64", True, PREFILL_SRC,
-     "145be21612b5eca3bbc8749990827d96b04fd454a2ce731779456ce90ce96e3b", 351610368),
+     "4b16b779af583ecbe033acd248a3aa91760027bc0fe100fa345cb03f55d3d09e", 351610368),
     ("prefill_f16", "prefill_f16_b4h32s4096d128_qk3", True, PREFILL_SRC,
-     "145be21612b5eca3bbc8749990827d96b04fd454a2ce731779456ce90ce96e3b", 521415424),
+     "4b16b779af583ecbe033acd248a3aa91760027bc0fe100fa345cb03f55d3d09e", 521415424),
     ("prefill_bf16", "prefill_varlen_bf16_b4h32s4096d128", True, PREFILL_SRC,
-     "145be21612b5eca3bbc8749990827d96b04fd454a2ce731779456ce90ce96e3b", 843763712),
+     "4b16b779af583ecbe033acd248a3aa91760027bc0fe100fa345cb03f55d3d09e", 843763712),
     # the split kernel's bytes plus the merge kernel's
     ("decode", DECODE_WORKLOAD, True, DECODE_SRC,
      "51a3bd6f99e0087d667f1f6f42c299a03ac35889771e1e3c211f81a163af275f", 1202752000),

@@ -71,6 +71,9 @@ def _declare(lib):
     lib.mha_decode_num_splits.restype = i
     lib.mha_prefill_wide_schedule.argtypes = [i, i, i, i, i, i, i]
     lib.mha_prefill_wide_schedule.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.mha_prefill_schedule.argtypes = [i, i, i, i, i, i, i, i, ip, ip, i]
+    lib.mha_prefill_schedule.restype = i
     lib.mha_get_device_status.argtypes = [vp]
     lib.mha_get_device_status.restype = i
     lib.mha_status_string.argtypes = [i]
@@ -364,6 +367,25 @@ def mha_prefill_wide_schedule(B: int, H: int, S: int, D: int, causal: bool = Tru
     if n < 0:
         raise MHAError(-n, "mha_prefill_wide_schedule")
     return n == 1
+
+
+def mha_prefill_schedule(B: int, H: int, S: int, D: int, causal: bool = True,
+                         key_padding: bool = False, sm_count: int = 0,
+                         cta: int = 0) -> list[tuple[int, int]]:
+    """The (b*H + h, 256-row query block) items CTA `cta` of a prefill launch
+    of this shape works on, in its order (host only)."""
+    lib = _load()
+    args = (int(B), int(H), int(S), int(D), int(bool(causal)), int(bool(key_padding)),
+            int(sm_count), int(cta))
+    n = lib.mha_prefill_schedule(*args, None, None, 0)
+    if n < 0:
+        raise MHAError(-n, "mha_prefill_schedule")
+    bh = (ctypes.c_int * max(n, 1))()
+    qp = (ctypes.c_int * max(n, 1))()
+    m = lib.mha_prefill_schedule(*args, bh, qp, n)
+    if m != n:
+        raise MHAError(1 if m >= 0 else -m, "mha_prefill_schedule")
+    return list(zip(bh[:n], qp[:n]))
 
 
 def mha_get_device_status(stream=None, device=None) -> int:

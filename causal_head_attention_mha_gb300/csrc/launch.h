@@ -61,6 +61,11 @@ int device_sm_count();
 // shape (see prefill_bf16.cu) on a grid of min(items, sm_count) CTAs.
 bool prefill_wide_schedule(int B, int H, int S, int D, bool causal, bool key_padding,
                            int sm_count);
+// The items (b*H + h, 256-row query block) CTA `cta` of such a launch works
+// on, in its order: up to `capacity` written to bh[] and qp[]; returns the
+// CTA's item count (0 outside the grid).
+int prefill_schedule_items(int B, int H, int S, int D, bool causal, bool key_padding,
+                           int sm_count, int cta, int* bh, int* qp, int capacity);
 
 // Keeps `e` for mha_last_cuda_error, clears it, and returns MHA_ERR_CUDA.
 int record_cuda_failure(cudaError_t e);

@@ -248,6 +248,18 @@ int mha_prefill_wide_schedule(int B, int H, int S, int D, int causal, int key_pa
   return mha::prefill_wide_schedule(B, H, S, D, causal != 0, key_padding != 0, sm_count) ? 1 : 0;
 }
 
+int mha_prefill_schedule(int B, int H, int S, int D, int causal, int key_padding, int sm_count,
+                         int cta, int* bh_out, int* qp_out, int capacity) {
+  if (B < 1 || H < 1 || S < 1 || (D != 64 && D != 128) || capacity < 0)
+    return -MHA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * S * D >= (1LL << 31)) return -MHA_ERR_INVALID_ARG;
+  if (capacity > 0 && (bh_out == nullptr || qp_out == nullptr)) return -MHA_ERR_INVALID_ARG;
+  if (sm_count <= 0) sm_count = mha::device_sm_count();
+  if (sm_count <= 0) return -MHA_ERR_CUDA;
+  return mha::prefill_schedule_items(B, H, S, D, causal != 0, key_padding != 0, sm_count, cta,
+                                     bh_out, qp_out, capacity);
+}
+
 int mha_get_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);

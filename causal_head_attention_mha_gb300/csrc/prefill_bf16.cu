@@ -1272,6 +1272,27 @@ bool prefill_wide_schedule(int B, int H, int S, int D, bool causal, bool key_pad
   return wide_schedule(n_qp, BH, S, causal, grid);
 }
 
+// The kernel's own Sched, walked on the host for one CTA of the launch.
+int prefill_schedule_items(int B, int H, int S, int D, bool causal, bool key_padding,
+                           int sm_count, int cta, int* bh_out, int* qp_out, int capacity) {
+  const bool wide = prefill_wide_schedule(B, H, S, D, causal, key_padding, sm_count);
+  const int BH = B * H;
+  const int n_qp = (S + 2 * BM - 1) / (2 * BM);
+  const long long items = static_cast<long long>(BH) * n_qp;
+  const int grid = static_cast<int>(items < sm_count ? items : sm_count);
+  if (cta < 0 || cta >= grid) return 0;
+  Sched sch(n_qp, BH, causal, wide, grid, cta);
+  int bh, qp, n = 0;
+  while (sch.next(bh, qp)) {
+    if (n < capacity) {
+      bh_out[n] = bh;
+      qp_out[n] = qp;
+    }
+    ++n;
+  }
+  return n;
+}
+
 cudaError_t launch_prefill_bf16(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 const int* key_lens, int B, int H, int S, int D, float scale,
                                 int causal, int o_layout, cudaStream_t stream,

@@ -225,6 +225,27 @@ int mha_prefill_wide_schedule(int B, int H, int S, int D, int causal, int key_pa
                               int sm_count);
 
 /*
+ * The work items of one CTA of the same launch, in the order it takes them:
+ * item i is the 256-row query block qp_out[i] (rows 256*qp .. 256*qp + 255)
+ * of head row bh_out[i] = b*H + h.  The grid is min(B*H*ceil(S/256),
+ * sm_count) CTAs and every (bh, qp) belongs to exactly one of them.
+ *
+ *   cta      : CTA index; outside [0, grid) the CTA has no items.
+ *   bh_out, qp_out : host int arrays of `capacity` entries (caller-owned;
+ *              may be NULL when capacity is 0); the first min(count,
+ *              capacity) items are written.
+ *   sm_count : as for mha_prefill_wide_schedule.
+ *
+ * Returns the CTA's item count (which may exceed capacity; call with
+ * capacity 0 to size the arrays), or a negative MHA_ERR_* code:
+ * -MHA_ERR_INVALID_ARG for a non-positive size, D other than 64 and 128,
+ * B*H*S*D >= 2^31, a negative capacity or NULL arrays with capacity > 0;
+ * -MHA_ERR_CUDA when the SM count cannot be read.  Host arithmetic only.
+ */
+int mha_prefill_schedule(int B, int H, int S, int D, int causal, int key_padding, int sm_count,
+                         int cta, int* bh_out, int* qp_out, int capacity);
+
+/*
  * Fused Q, K, V projection feeding the attention calls: page 3 section 2
  * (Q = X W_Q, K = X W_K, V = X W_V) with its section 2.1 shapes, the three
  * products fused into one GEMM as page 1 section 2.1 ("Week 4 CUDA notes")

@@ -207,3 +207,81 @@ def test_prefill_schedule_choice_fixed_cases_and_errors(lib):
     assert lib.mha_prefill_wide_schedule(1, 1, 256, 128, 1, 0, 152) in (0, 1)
     for bad in ((0, 32, 4096, 128), (4, 0, 4096, 128), (4, 32, 0, 128), (4, 32, 4096, 96)):
         assert lib.mha_prefill_wide_schedule(*bad, 1, 0, 152) == -INVALID
+
+
+# ------------------------------------------------------------------ the prefill's item schedule
+def _items(B, H, S, D, causal, key_padding, sm=152):
+    """Every CTA's items through the binding: {cta: [(bh, qp), ...]}."""
+    from causal_head_attention_mha_gb300 import binding
+    n_qp = -(-S // 256)
+    grid = min(B * H * n_qp, sm)
+    return {c: binding.mha_prefill_schedule(B, H, S, D, causal, key_padding, sm, c)
+            for c in range(grid)}, grid, n_qp
+
+
+@pytest.mark.parametrize("B,H,S,D,causal,key_padding,bound", [
+    (4, 32, 4096, 128, True, False, 1.03),    # narrow groups, causal (1.028)
+    (4, 32, 4096, 128, False, False, 1.04),   # narrow groups: 2048 equal items (1.039)
+    (1, 32, 2048, 128, True, False, 1.07),    # 256 items for 152 CTAs (1.062)
+    (2, 16, 16384, 64, True, False, 1.01),    # D = 64: wide groups (1.002)
+    (2, 16, 16384, 128, True, False, 1.01),   # wide, chosen by the load model (1.002)
+    (2, 16, 16384, 128, False, False, 1.04),  # (1.039)
+    (1, 32, 8192, 128, False, False, 1.04),   # (1.039)
+    (8, 40, 600, 128, True, False, 1.16),     # ragged: the last block has one tile (1.154)
+    (4, 32, 4096, 128, True, True, 1.01),     # key padding: wide groups (1.005)
+    (3, 5, 77, 64, True, False, 1.0),         # fewer items than SMs: one each
+    (64, 32, 4096, 128, True, False, 1.01),   # 32768 items, many groups (1.001)
+])
+def test_prefill_schedule_deals_every_item_once(lib, B, H, S, D, causal, key_padding, bound):
+    per_cta, grid, n_qp = _items(B, H, S, D, causal, key_padding)
+    seen = {}
+    for c, items in per_cta.items():
+        for it in items:
+            assert it not in seen, f"item {it} dealt to CTAs {seen[it]} and {c}"
+            seen[it] = c
+    assert set(seen) == {(bh, qp) for bh in range(B * H) for qp in range(n_qp)}
+    # no CTA past the grid, and every CTA of the grid has work
+    from causal_head_attention_mha_gb300 import binding
+    assert binding.mha_prefill_schedule(B, H, S, D, causal, key_padding, 152, grid) == []
+    assert all(per_cta[c] for c in range(grid))
+    # the busiest CTA's load (key tiles of its items plus two per item) against
+    # the average, as the host's load model computes it when it picks the
+    # group shape (the figure in brackets)
+    def load(bh, qp):
+        n_kt = -(-S // 128)
+        nA = min(2 * qp + 1, n_kt) if causal else n_kt
+        hasB = (2 * qp + 1) * 128 < S
+        nB = (min(2 * qp + 2, n_kt) if causal else n_kt) if hasB else 0
+        return nA + nB + 2
+    loads = [sum(load(*it) for it in per_cta[c]) for c in range(grid)]
+    assert max(loads) * grid <= bound * sum(loads) + 1e-9
+
+
+def test_prefill_schedule_takes_heavy_blocks_first(lib):
+    """Causal: within a group of heads a CTA's blocks come in decreasing order
+    (the later query blocks, with more key tiles, first)."""
+    per_cta, grid, n_qp = _items(4, 32, 4096, 128, True, False)
+    for c in range(grid):
+        qps = [qp for _, qp in per_cta[c]]
+        # narrow groups: two items per CTA per group, heavy then light
+        for i in range(0, len(qps) - 1, 2):
+            assert qps[i] >= qps[i + 1]
+
+
+def test_prefill_schedule_errors(lib):
+    from causal_head_attention_mha_gb300 import binding
+    ip = ctypes.POINTER(ctypes.c_int)
+    for bad in ((0, 32, 4096, 128), (4, 0, 4096, 128), (4, 32, 0, 128), (4, 32, 4096, 96),
+                (1024, 1024, 4096, 128)):    # B*H*S*D >= 2^31
+        assert lib.mha_prefill_schedule(*bad, 1, 0, 152, 0, None, None, 0) == -INVALID
+    assert lib.mha_prefill_schedule(4, 32, 4096, 128, 1, 0, 152, 0, None, None, -1) == -INVALID
+    assert lib.mha_prefill_schedule(4, 32, 4096, 128, 1, 0, 152, 0, None, None, 4) == -INVALID
+    # a capacity below the count writes only that many and still returns the count
+    n = lib.mha_prefill_schedule(4, 32, 4096, 128, 1, 0, 152, 3, None, None, 0)
+    assert n > 2
+    bh = (ctypes.c_int * 3)(-1, -1, -1)
+    qp = (ctypes.c_int * 3)(-1, -1, -1)
+    assert lib.mha_prefill_schedule(4, 32, 4096, 128, 1, 0, 152, 3, bh, qp, 2) == n
+    full = binding.mha_prefill_schedule(4, 32, 4096, 128, True, False, 152, 3)
+    assert [(bh[0], qp[0]), (bh[1], qp[1])] == full[:2] and bh[2] == -1 and qp[2] == -1
+    assert lib.mha_prefill_schedule(4, 32, 4096, 128, 1, 0, 152, -1, None, None, 0) == 0
