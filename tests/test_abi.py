@@ -285,3 +285,14 @@ def test_prefill_schedule_errors(lib):
     full = binding.mha_prefill_schedule(4, 32, 4096, 128, True, False, 152, 3)
     assert [(bh[0], qp[0]), (bh[1], qp[1])] == full[:2] and bh[2] == -1 and qp[2] == -1
     assert lib.mha_prefill_schedule(4, 32, 4096, 128, 1, 0, 152, -1, None, None, 0) == 0
+
+
+def test_prefill_schedule_binding_raises(lib):
+    from causal_head_attention_mha_gb300 import binding
+    with pytest.raises(binding.MHAError):
+        binding.mha_prefill_schedule(4, 32, 4096, 96, True, False, 152, 0)
+    with pytest.raises(binding.MHAError):
+        binding.mha_prefill_schedule(0, 32, 4096, 128, True, False, 152, 0)
+    # one CTA per item when there are fewer items than SMs
+    assert binding.mha_prefill_schedule(1, 1, 256, 128, True, False, 152, 0) == [(0, 0)]
+    assert binding.mha_prefill_schedule(1, 1, 256, 128, True, False, 152, 1) == []
